@@ -1,0 +1,227 @@
+/*
+ * akv.h — C ABI of libakv: the AKV hot path (attention over an active KV
+ * cache shaped by append / drop / repos) on NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Cache Engineering for Agents" (arXiv 2610.28577), as restated by
+ * the paper review page (sections 3.3-3.4, 4, 4.2, Appendix A.1.1-A.1.2) and
+ * by the explainer page (sections 1-4, the system README).
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer.  No entry point allocates device memory;
+ *    calls that need scratch take a caller-provided workspace whose size is
+ *    returned by the matching *_workspace* query.  Workspaces must be 256-byte
+ *    aligned.
+ *  - Pointers documented "device" are CUDA device (or managed) pointers;
+ *    "host" pointers are read synchronously during the call and may be
+ *    reused as soon as the call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  Arguments are validated before any
+ *    launch: on AKV_ERR_INVALID / AKV_ERR_UNSUPPORTED / AKV_ERR_WORKSPACE
+ *    nothing was enqueued.  AKV_ERR_CUDA reports a failed runtime call or
+ *    launch.  Kernels that wait on barriers do so with an iteration limit;
+ *    when one gives up it sets a bit in the workspace status word (see
+ *    akv_workspace_status) instead of hanging or trapping.
+ *  - Tensors are token-major and row-major: Q [T, Hq, D], K and V [T, Hkv, D].
+ *    Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *  - dtype AKV_F32 or AKV_BF16; arithmetic accumulates in fp32.  D must be
+ *    64, Hq % Hkv == 0.  RoPE pairs coordinate i with i + D/2 and turns the
+ *    pair by the angle p * rope_base^(-2i/D); scores are scaled by 1/sqrt(D).
+ *  - akv_last_error() returns a thread-local message for the last non-OK
+ *    status returned on the calling thread.
+ */
+#ifndef AKV_H_
+#define AKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *akv_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  AKV_OK = 0,
+  AKV_ERR_INVALID = 1,     /* bad argument or op log; nothing enqueued */
+  AKV_ERR_CUDA = 2,        /* CUDA runtime call or kernel launch failed */
+  AKV_ERR_WORKSPACE = 3,   /* workspace too small or misaligned */
+  AKV_ERR_UNSUPPORTED = 4, /* valid request the kernels do not implement */
+  AKV_ERR_DEVICE = 5       /* a kernel reported failure via the status word */
+} akv_status;
+
+typedef enum { AKV_F32 = 0, AKV_BF16 = 1 } akv_dtype;
+
+/* One request's cache-operation log in operate-after form (paper review page,
+ * section 4 and Figure 6; explainer page section 4, system README).
+ * All arrays are host memory.
+ *   msg_start   [n_msgs + 1] token CSR: message m holds tokens
+ *               msg_start[m] .. msg_start[m+1]-1 (logical order), msg_start[0]
+ *               = 0, non-decreasing.  Every message is an implicit append.
+ *   drop_after, drop_target  [n_drops]: after message drop_after[i] ends, the
+ *               KV of message drop_target[i] leaves the active cache
+ *               (drop(P), section 3.3).  0 <= drop_target[i] <= drop_after[i]
+ *               < n_msgs.  Dropping an already dropped message is a no-op.
+ *   repos_after [n_repos]: after that message ends, the survivors are
+ *               renumbered 0..r-1 in logical order (repos, section 3.3).
+ *               0 <= repos_after[j] < n_msgs; duplicates are a no-op.
+ * At one boundary all drops act before the repos. */
+typedef struct {
+  int32_t n_msgs;
+  const int32_t *msg_start;
+  int32_t n_drops;
+  const int32_t *drop_after;
+  const int32_t *drop_target;
+  int32_t n_repos;
+  const int32_t *repos_after;
+} akv_oplog;
+
+typedef struct {
+  int32_t Hq, Hkv, D;
+  akv_dtype dtype;
+  float rope_base;
+} akv_shape;
+
+const char *akv_last_error(void);
+const char *akv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Segment-batch restoration prefill (paper review page section 4.2,
+ * Appendix A.1.1, Figure 10): queries are cut at every boundary carrying a
+ * drop or repos; each segment attends causally over its own tokens and the
+ * still-active KV of earlier segments, so a dropped entry stays visible to
+ * the segments before its drop and is hidden from later ones.  Keys are read
+ * at the positions of the version current during the query's segment (the
+ * temporary per-segment KV versions of A.1.1).  Equivalently, token t attends
+ * over the active cache at its append time (sequential replay, section 3.4).
+ * ---------------------------------------------------------------------- */
+
+typedef struct akv_plan akv_plan;
+
+/* Plan a batch of n_req requests on the host (validation, segments, key
+ * versions, visibility tile lists).  cu_seqlens: host [n_req + 1], request b
+ * owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of Q/K/V/out and must have
+ * cu_seqlens[b+1]-cu_seqlens[b] == ops[b].msg_start[ops[b].n_msgs].
+ * logical_idx: host [T] or NULL; when given, row cu_seqlens[b]+i must carry
+ * logical index i (rows are in logical order).  On success *plan_out owns a
+ * host object released with akv_plan_destroy.  Returns AKV_ERR_INVALID for a
+ * bad op log (target later than its boundary, index out of range, ...). */
+akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                           const int32_t *logical_idx, const akv_oplog *ops,
+                           akv_plan **plan_out);
+void akv_plan_destroy(akv_plan *plan);
+
+typedef struct {
+  int64_t T;              /* rows in the batch */
+  int64_t n_qtiles;       /* 128-row query tiles (never straddle a request or version) */
+  int64_t n_windows;      /* 128-key windows over all tiles */
+  int64_t n_full_windows; /* windows that need no in-tile mask */
+  int64_t visible_pairs;  /* sum over rows of visible keys (one head) */
+  int64_t n_segments;     /* over all requests */
+  int32_t max_versions;   /* key versions (1 + repos count) of the largest request */
+  int32_t reserved;
+  size_t workspace_bytes; /* for akv_segment_attention_run / _visible_counts */
+} akv_plan_info;
+
+akv_status akv_plan_get_info(const akv_plan *plan, akv_plan_info *info);
+
+/* Per-row integer tables of the plan (host outputs, each [T], values
+ * request-relative): append position, segment, key version, and the first
+ * segment that no longer sees the row's key (INT32_MAX if never dropped). */
+akv_status akv_plan_tables(const akv_plan *plan, int32_t *tok_pos, int32_t *tok_seg,
+                           int32_t *tok_ver, int32_t *drop_seg);
+
+/* Run a planned prefill.  q [T,Hq,D], k/v [T,Hkv,D]: device, raw (not
+ * rotated).  out [T,Hq,D] device.  workspace: device, >= workspace_bytes of
+ * the plan info.  The plan tables are copied into the workspace by this call
+ * (host -> device on `stream`); the plan may be destroyed once it returns. */
+akv_status akv_segment_attention_run(const akv_plan *plan, const void *q, const void *k,
+                                     const void *v, void *out, void *workspace,
+                                     size_t workspace_bytes, akv_stream_t stream);
+
+/* The two halves of a run, for callers that time or overlap them:
+ * akv_segment_prepare uploads the plan tables and writes the rotated and
+ * permuted copies (the per-segment temporary KV versions of Appendix A.1.1)
+ * into the workspace; akv_segment_attend then runs the attention over them.
+ * prepare + attend on one stream == run. */
+akv_status akv_segment_prepare(const akv_plan *plan, const void *q, const void *k, const void *v,
+                               void *workspace, size_t workspace_bytes, akv_stream_t stream);
+akv_status akv_segment_attend(const akv_plan *plan, void *out, void *workspace,
+                              size_t workspace_bytes, akv_stream_t stream);
+
+/* One-shot form: plan, then run.  Same arguments as the two calls above. */
+size_t akv_segment_attention_workspace(const akv_shape *shape, int32_t n_req,
+                                       const int32_t *cu_seqlens, const akv_oplog *ops);
+akv_status akv_segment_attention(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                                 const int32_t *logical_idx, const akv_oplog *ops, const void *q,
+                                 const void *k, const void *v, void *out, void *workspace,
+                                 size_t workspace_bytes, akv_stream_t stream);
+
+/* Visibility as the attention kernels see it: counts[t] (device int32 [T]) =
+ * number of keys row t attends over, enumerated through the plan's key
+ * windows and the in-tile mask predicate.  Equals the size of the active
+ * cache at the row's append time.  Uses the same workspace as a run. */
+akv_status akv_segment_visible_counts(const akv_plan *plan, int32_t *counts, void *workspace,
+                                      size_t workspace_bytes, akv_stream_t stream);
+
+/* Reads and clears the status word at the start of a workspace used by the
+ * calls above (synchronises `stream`).  *code = 0 when no kernel reported a
+ * failure; otherwise a bit mask and the call returns AKV_ERR_DEVICE:
+ *   1  a barrier wait in a kernel gave up (its outputs are not valid);
+ *   2  (bf16) a rotated query or key exceeded the fp16 range of the score
+ *      operands (|value| > 65504) and was saturated. */
+akv_status akv_workspace_status(void *workspace, akv_stream_t stream, uint32_t *code);
+
+/* ------------------------------------------------------------------------
+ * Compaction (drop, section 3.3; active vs logical trajectory, explainer
+ * section 1): the active cache right after the drops of boundary `upto`
+ * (-1: the last message), as ascending logical indices active_idx[0..n) and
+ * their positions active_pos[0..n) in the version current before any repos
+ * listed at `upto` (a repos there moves the j-th survivor to position j).
+ * T must equal ops->msg_start[ops->n_msgs].  active_idx/active_pos: device
+ * int32 [T] (the first *n_active entries are written).  *n_active: host,
+ * known when the call returns. */
+size_t akv_compact_workspace(const akv_oplog *ops, int32_t T);
+akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *active_idx,
+                       int32_t *active_pos, int32_t *n_active, void *workspace,
+                       size_t workspace_bytes, akv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Repos / position-version conversion (section 3.3, section 4.2 and
+ * Appendix A.1.2): for j in 0..r-1, K_out[j] = R(pos_to[j] - pos_from[j]) *
+ * K_in[src_idx[j]] and V_out[j] = V_in[src_idx[j]] (values are copied
+ * unchanged).  k_in/v_in: device [*, Hkv, D], keys already rotated at
+ * pos_from.  src_idx, pos_from: device int32 [r]; pos_to: device int32 [r] or
+ * NULL for pos_to[j] = j (the renumbering 0..r-1 of a repos).  k_out/v_out:
+ * device [r, Hkv, D]; they must not overlap the inputs. */
+akv_status akv_repos_rotate(const akv_shape *shape, int32_t r, const int32_t *src_idx,
+                            const int32_t *pos_from, const int32_t *pos_to, const void *k_in,
+                            const void *v_in, void *k_out, void *v_out, akv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Decode over the active cache (paper review page section 4 serving flow,
+ * "decode reads only the active cache"; system README: drop/repos support
+ * page size 1).  Request b's query q[b] (raw [Hq, D]) is rotated at
+ * q_pos[b] and attends over pool slots kv_indices[kv_indptr[b] ..
+ * kv_indptr[b+1]) of k_pool/v_pool ([S, Hkv, D], keys stored already
+ * rotated).  q_pos, kv_indptr ([B+1]), kv_indices: device int32.  max_kv:
+ * host, an upper bound on any request's length (sizes the split-KV grid).
+ * out [B, Hq, D] device.  A request with no keys gets zeros. */
+size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
+akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
+                                const int32_t *q_pos, const void *k_pool, const void *v_pool,
+                                const int32_t *kv_indptr, const int32_t *kv_indices,
+                                int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
+                                akv_stream_t stream);
+
+/* Append (section 3.3): for i in 0..n-1, k_pool[slot[i]] = R(pos[i]) *
+ * k_new[i] and v_pool[slot[i]] = v_new[i].  k_new/v_new: device [n, Hkv, D]
+ * raw; pos, slot: device int32 [n]; slots must be distinct. */
+akv_status akv_append_kv(const akv_shape *shape, int32_t n, const void *k_new, const void *v_new,
+                         const int32_t *pos, const int32_t *slot, void *k_pool, void *v_pool,
+                         akv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AKV_H_ */

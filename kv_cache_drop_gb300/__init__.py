@@ -1,0 +1,314 @@
+"""Python binding of libakv, the GB300 (sm_103a) AKV hot path.
+
+Argument marshalling only: every function below forwards to the C entry point
+of the same name in ``libakv.so`` (declared in ``include/akv.h``), passing
+device pointers of torch tensors, host arrays of the op logs and the current
+CUDA stream.  There is no fallback: if the library is missing or a call
+fails, an exception is raised.
+
+Op logs are passed per request as ``(msg_start, drop_after, drop_target,
+repos_after)`` integer arrays in the operate-after form of the pages'
+request grammar (drop the KV of message ``drop_target[i]`` after message
+``drop_after[i]`` ends; re-position after ``repos_after[j]``; drops before
+the repos at one boundary).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libakv.so")
+
+AKV_F32, AKV_BF16 = 0, 1
+_STATUS = {0: "AKV_OK", 1: "AKV_ERR_INVALID", 2: "AKV_ERR_CUDA", 3: "AKV_ERR_WORKSPACE",
+           4: "AKV_ERR_UNSUPPORTED", 5: "AKV_ERR_DEVICE"}
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+class AkvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+
+
+class OpLog(ctypes.Structure):
+    _fields_ = [("n_msgs", ctypes.c_int32), ("msg_start", _i32p),
+                ("n_drops", ctypes.c_int32), ("drop_after", _i32p), ("drop_target", _i32p),
+                ("n_repos", ctypes.c_int32), ("repos_after", _i32p)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("n_qtiles", ctypes.c_int64),
+                ("n_windows", ctypes.c_int64), ("n_full_windows", ctypes.c_int64),
+                ("visible_pairs", ctypes.c_int64), ("n_segments", ctypes.c_int64),
+                ("max_versions", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
+_lib = None
+
+_SIGS = {
+    "akv_last_error": (ctypes.c_char_p, []),
+    "akv_version": (ctypes.c_char_p, []),
+    "akv_plan_create": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32, _i32p, _i32p,
+                                       ctypes.POINTER(OpLog), ctypes.POINTER(ctypes.c_void_p)]),
+    "akv_plan_destroy": (None, [ctypes.c_void_p]),
+    "akv_plan_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PlanInfo)]),
+    "akv_plan_tables": (ctypes.c_int, [ctypes.c_void_p, _i32p, _i32p, _i32p, _i32p]),
+    "akv_segment_attention_run": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 5 +
+                                  [ctypes.c_size_t, ctypes.c_void_p]),
+    "akv_segment_prepare": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_size_t,
+                                                                   ctypes.c_void_p]),
+    "akv_segment_attend": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_size_t,
+                                                                  ctypes.c_void_p]),
+    "akv_segment_attention_workspace": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int32,
+                                                          _i32p, ctypes.POINTER(OpLog)]),
+    "akv_segment_attention": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32, _i32p, _i32p,
+                                             ctypes.POINTER(OpLog)] + [ctypes.c_void_p] * 5 +
+                              [ctypes.c_size_t, ctypes.c_void_p]),
+    "akv_segment_visible_counts": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_size_t,
+                                                  ctypes.c_void_p]),
+    "akv_workspace_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.POINTER(ctypes.c_uint32)]),
+    "akv_compact_workspace": (ctypes.c_size_t, [ctypes.POINTER(OpLog), ctypes.c_int32]),
+    "akv_compact": (ctypes.c_int, [ctypes.POINTER(OpLog), ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_void_p, ctypes.c_void_p, _i32p, ctypes.c_void_p,
+                                   ctypes.c_size_t, ctypes.c_void_p]),
+    "akv_repos_rotate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
+                         [ctypes.c_void_p] * 7 + [ctypes.c_void_p]),
+    "akv_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int32,
+                                               ctypes.c_int32]),
+    "akv_decode_attention": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
+                             [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_void_p,
+                                                      ctypes.c_void_p, ctypes.c_size_t,
+                                                      ctypes.c_void_p]),
+    "akv_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
+                      [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),
+}
+
+EXPORTED = sorted(_SIGS)
+
+
+def lib():
+    """Load libakv.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libakv.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise AkvError(status, lib().akv_last_error().decode())
+
+
+def _dtype_code(dtype) -> int:
+    import torch
+    if dtype in ("f32", torch.float32, AKV_F32):
+        return AKV_F32
+    if dtype in ("bf16", torch.bfloat16, AKV_BF16):
+        return AKV_BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def shape(Hq: int, Hkv: int, D: int = 64, dtype="bf16", rope_base: float = 10000.0) -> Shape:
+    return Shape(Hq, Hkv, D, _dtype_code(dtype), rope_base)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class _Ops:
+    """Keeps the numpy arrays of a batch of op logs alive for a C call."""
+
+    def __init__(self, ops):
+        self.keep = []
+        self.arr = (OpLog * max(1, len(ops)))()
+        for i, (ms, da, dt, ra) in enumerate(ops):
+            ms, da, dt, ra = _i32(ms), _i32(da), _i32(dt), _i32(ra)
+            self.keep += [ms, da, dt, ra]
+            self.arr[i] = OpLog(len(ms) - 1, ms.ctypes.data_as(_i32p), len(da),
+                                da.ctypes.data_as(_i32p), dt.ctypes.data_as(_i32p), len(ra),
+                                ra.ctypes.data_as(_i32p))
+
+    def ptr(self, i: int = 0):
+        return ctypes.pointer(self.arr[i])
+
+    @property
+    def base(self):
+        return ctypes.cast(self.arr, ctypes.POINTER(OpLog))
+
+
+def _dev(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """Host plan of a segment-batch restoration prefill (akv_plan_create)."""
+
+    def __init__(self, shp: Shape, cu_seqlens, ops, logical_idx=None):
+        self._lib = lib()
+        self.shape = shp
+        self._ops = _Ops(ops)
+        cu = _i32(cu_seqlens)
+        li = None if logical_idx is None else _i32(logical_idx)
+        h = ctypes.c_void_p()
+        _check(self._lib.akv_plan_create(ctypes.byref(shp), len(ops), cu.ctypes.data_as(_i32p),
+                                         None if li is None else li.ctypes.data_as(_i32p),
+                                         self._ops.base, ctypes.byref(h)))
+        self.handle = h
+        info = PlanInfo()
+        _check(self._lib.akv_plan_get_info(h, ctypes.byref(info)))
+        self.info = info.as_dict()
+
+    def tables(self):
+        T = self.info["T"]
+        out = [np.empty(T, dtype=np.int32) for _ in range(4)]
+        _check(self._lib.akv_plan_tables(self.handle, *[o.ctypes.data_as(_i32p) for o in out]))
+        return dict(tok_pos=out[0], tok_seg=out[1], tok_ver=out[2], drop_seg=out[3])
+
+    def workspace(self, device="cuda"):
+        import torch
+        return torch.empty(max(1, self.info["workspace_bytes"]), dtype=torch.uint8, device=device)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            self._lib.akv_plan_destroy(h)
+            self.handle = None
+
+
+def akv_plan_create(shp: Shape, cu_seqlens, ops, logical_idx=None) -> Plan:
+    return Plan(shp, cu_seqlens, ops, logical_idx)
+
+
+def akv_segment_attention_run(plan: Plan, q, k, v, out, workspace, stream=None):
+    _check(lib().akv_segment_attention_run(plan.handle, _dev(q), _dev(k), _dev(v), _dev(out),
+                                           _dev(workspace), workspace.numel(), _stream(stream)))
+
+
+def akv_segment_prepare(plan: Plan, q, k, v, workspace, stream=None):
+    _check(lib().akv_segment_prepare(plan.handle, _dev(q), _dev(k), _dev(v), _dev(workspace),
+                                     workspace.numel(), _stream(stream)))
+
+
+def akv_segment_attend(plan: Plan, out, workspace, stream=None):
+    _check(lib().akv_segment_attend(plan.handle, _dev(out), _dev(workspace), workspace.numel(),
+                                    _stream(stream)))
+
+
+def akv_segment_attention_workspace(shp: Shape, cu_seqlens, ops) -> int:
+    o = _Ops(ops)
+    cu = _i32(cu_seqlens)
+    return lib().akv_segment_attention_workspace(ctypes.byref(shp), len(ops),
+                                                 cu.ctypes.data_as(_i32p), o.base)
+
+
+def akv_segment_attention(shp: Shape, cu_seqlens, logical_idx, ops, q, k, v, out, workspace,
+                          stream=None):
+    o = _Ops(ops)
+    cu = _i32(cu_seqlens)
+    li = None if logical_idx is None else _i32(logical_idx)
+    _check(lib().akv_segment_attention(ctypes.byref(shp), len(ops), cu.ctypes.data_as(_i32p),
+                                       None if li is None else li.ctypes.data_as(_i32p), o.base,
+                                       _dev(q), _dev(k), _dev(v), _dev(out), _dev(workspace),
+                                       workspace.numel(), _stream(stream)))
+
+
+def akv_segment_visible_counts(plan: Plan, counts, workspace, stream=None):
+    _check(lib().akv_segment_visible_counts(plan.handle, _dev(counts), _dev(workspace),
+                                            workspace.numel(), _stream(stream)))
+
+
+def akv_workspace_status(workspace, stream=None) -> int:
+    code = ctypes.c_uint32(0)
+    st = lib().akv_workspace_status(_dev(workspace), _stream(stream), ctypes.byref(code))
+    if st not in (0, 5):
+        _check(st)
+    return code.value
+
+
+def akv_compact_workspace(ops, T: int) -> int:
+    o = _Ops([ops])
+    return lib().akv_compact_workspace(o.ptr(), T)
+
+
+def akv_compact(ops, T: int, upto: int, active_idx, active_pos, workspace, stream=None) -> int:
+    o = _Ops([ops])
+    n = ctypes.c_int32(0)
+    _check(lib().akv_compact(o.ptr(), T, upto, _dev(active_idx), _dev(active_pos),
+                             ctypes.byref(n), _dev(workspace),
+                             0 if workspace is None else workspace.numel(), _stream(stream)))
+    return n.value
+
+
+def akv_repos_rotate(shp: Shape, r: int, src_idx, pos_from, pos_to, k_in, v_in, k_out, v_out,
+                     stream=None):
+    _check(lib().akv_repos_rotate(ctypes.byref(shp), r, _dev(src_idx), _dev(pos_from),
+                                  _dev(pos_to), _dev(k_in), _dev(v_in), _dev(k_out), _dev(v_out),
+                                  _stream(stream)))
+
+
+def akv_decode_workspace(shp: Shape, B: int, max_kv: int) -> int:
+    return lib().akv_decode_workspace(ctypes.byref(shp), B, max_kv)
+
+
+def akv_decode_attention(shp: Shape, B: int, q, q_pos, k_pool, v_pool, kv_indptr, kv_indices,
+                         max_kv: int, out, workspace, stream=None):
+    _check(lib().akv_decode_attention(ctypes.byref(shp), B, _dev(q), _dev(q_pos), _dev(k_pool),
+                                      _dev(v_pool), _dev(kv_indptr), _dev(kv_indices), max_kv,
+                                      _dev(out), _dev(workspace),
+                                      0 if workspace is None else workspace.numel(),
+                                      _stream(stream)))
+
+
+def akv_append_kv(shp: Shape, n: int, k_new, v_new, pos, slot, k_pool, v_pool, stream=None):
+    _check(lib().akv_append_kv(ctypes.byref(shp), n, _dev(k_new), _dev(v_new), _dev(pos),
+                               _dev(slot), _dev(k_pool), _dev(v_pool), _stream(stream)))
+
+
+def to_device(arr: np.ndarray, dtype: str, device="cuda"):
+    """numpy float32 array or bf16 bit patterns (uint16) -> torch tensor on device."""
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(device).view(
+            torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+def i32_device(a, device="cuda"):
+    import torch
+    return torch.from_numpy(_i32(a)).to(device)

@@ -1,0 +1,99 @@
+// Internal declarations shared by the host planner / C ABI and the CUDA
+// launchers.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "akv.h"
+
+namespace akv {
+
+constexpr int kD = 64;          // head dim supported by every kernel
+constexpr int kTileQ = 128;     // query rows per tile (tcgen05 M)
+constexpr int kTileK = 128;     // keys per window (tcgen05 N of Q K^T)
+constexpr int kSlotPad = 128;   // padding entries after the slot tables
+constexpr uint32_t kWinFull = 0x80000000u;  // window flag: no in-tile mask needed
+constexpr uint32_t kStatusWaitTimeout = 1u; // status bit: a barrier wait gave up
+constexpr uint32_t kStatusFp16Range = 2u;   // status bit: a rotated Q/K value exceeded fp16
+
+// One query tile: rows [t0, t0+len) of one request, all in one key version.
+struct QTile {
+  int32_t t0;       // first row (batch-global)
+  int32_t len;      // 1..kTileQ
+  int32_t ver;      // key version read by these rows
+  int32_t req;      // request index
+  int32_t win_off;  // first entry in the window array
+  int32_t win_cnt;  // number of 128-key windows
+  int32_t seg_lo;   // segment of row t0 (request-relative)
+  int32_t seg_hi;   // segment of the last row
+};
+static_assert(sizeof(QTile) == 32, "QTile layout");
+
+// Device views of the plan tables and the rotated copies, all inside one
+// caller workspace.
+struct PlanDev {
+  uint32_t *status;          // workspace status word
+  const int32_t *tok_qpos;   // [T] query position (append position) of each row
+  const int32_t *tok_seg;    // [T] segment of each row
+  const int32_t *slot_src;   // [T] permuted key slot -> source row
+  const int32_t *slot_u;     // [T+pad] permuted key slot -> batch-global logical row (pad INT_MAX)
+  const int32_t *slot_dseg;  // [T+pad] first segment that no longer sees the slot (pad INT_MIN)
+  const int32_t *slot_pos;   // [max_ver][T] position of the slot's key in each version
+  const QTile *qtiles;       // [n_qtiles]
+  const uint32_t *windows;   // [n_windows] slot start | kWinFull
+  const int32_t *order;      // [n_qtiles] tiles by decreasing window count
+  void *qr;                  // [Hq][T][D]  rotated queries, head-major (fp16 for bf16 inputs)
+  void *kr;                  // [max_ver][Hkv][T][D] rotated keys, permuted slots, head-major
+                             // (fp16 for bf16 inputs)
+  void *vp;                  // [Hkv][T][D] values, permuted slots, head-major
+  int64_t T;
+  int32_t n_qtiles;
+  int32_t max_ver;
+  int32_t Hq, Hkv;
+  float rope_base;
+  int32_t dtype;             // akv_dtype
+};
+
+// RoPE frequencies theta_i = base^(-2i/D), computed in double on the host.
+struct RopeTheta {
+  double th[kD / 2];
+};
+
+void rope_theta(float base, RopeTheta *out);
+
+// ---- launchers (defined in the .cu files) ----
+cudaError_t launch_prep(const PlanDev &p, const void *q, const void *k, const void *v,
+                        const RopeTheta &th, cudaStream_t s);
+cudaError_t launch_attn_simt_f32(const PlanDev &p, void *out, cudaStream_t s);
+cudaError_t launch_visible_counts(const PlanDev &p, int32_t *counts, cudaStream_t s);
+cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s);
+cudaError_t launch_repos(int dtype, int Hkv, int r, const int32_t *src, const int32_t *pf,
+                         const int32_t *pt, const void *kin, const void *vin, void *kout,
+                         void *vout, const RopeTheta &th, cudaStream_t s);
+cudaError_t launch_append(int dtype, int Hkv, int n, const void *kn, const void *vn,
+                          const int32_t *pos, const int32_t *slot, void *kp, void *vp,
+                          const RopeTheta &th, cudaStream_t s);
+
+struct CompactDev {
+  const int32_t *msg_start;  // [n_msgs+1]
+  const uint8_t *keep;       // [n_msgs] message survives the drops up to the boundary
+  const uint8_t *alive_br;   // [n_msgs] message alive right after the last earlier repos
+  int32_t *block_cnt;        // [2 * n_blocks] kept / alive counts per block
+  int32_t n_msgs;
+  int32_t T;                 // tokens in messages <= boundary
+  int32_t br_end;            // first token after the last earlier repos (0 if none)
+  int32_t r;                 // survivors at that repos
+  int32_t has_br;
+};
+cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *active_pos,
+                           cudaStream_t s);
+int compact_blocks(int T);
+
+size_t decode_partials_bytes(int B, int Hq, int max_kv);
+cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, const int32_t *qpos,
+                          const void *kp, const void *vp, const int32_t *indptr,
+                          const int32_t *indices, int max_kv, void *out, void *ws,
+                          const RopeTheta &th, cudaStream_t s);
+
+}  // namespace akv

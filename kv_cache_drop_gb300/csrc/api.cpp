@@ -1,0 +1,739 @@
+// C ABI of libakv: argument validation, the host planner for segment-batch
+// restoration, workspace layout, and kernel orchestration.
+//
+// The planner restates "Cache Engineering for Agents" (paper review page,
+// section 3.3 cache operations, section 4 operate-after grammar / Figure 6,
+// section 4.2 and Appendix A.1.1 segment-batch attention):
+//  * a segment ends at every boundary that lists a drop or a repos;
+//  * row t (segment seg(t)) sees key u iff u <= t and seg(t) < drop_seg(u),
+//    where drop_seg(u) is the segment right after the boundary that first
+//    drops u's message;
+//  * every repos opens a new key version: the survivors are renumbered
+//    0..r-1 in logical order and later appends continue from r; rows read
+//    keys at the positions of their own version.
+// Key slots are permuted once per request so that keys with the same drop
+// segment are contiguous (never-dropped keys first, then by decreasing drop
+// segment, logical order inside): the keys a query tile can see then form a
+// few long runs instead of one run per surviving message, and the attention
+// kernels cover them with 128-key windows.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "akv_internal.h"
+
+using namespace akv;
+
+namespace {
+
+thread_local std::string g_err;
+
+akv_status fail(akv_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+akv_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(AKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// AKV_FAULT=invalid|cuda|workspace makes entry points fail before launching
+// anything, so callers can exercise their error paths without a GPU fault.
+akv_status injected_fault(const char *entry) {
+  static const char *f = getenv("AKV_FAULT");
+  if (!f || !*f) return AKV_OK;
+  if (!strcmp(f, "invalid")) return fail(AKV_ERR_INVALID, "%s: injected fault", entry);
+  if (!strcmp(f, "cuda")) return fail(AKV_ERR_CUDA, "%s: injected fault", entry);
+  if (!strcmp(f, "workspace")) return fail(AKV_ERR_WORKSPACE, "%s: injected fault", entry);
+  return AKV_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t esize(akv_dtype d) { return d == AKV_F32 ? 4 : 2; }
+
+akv_status check_shape(const akv_shape *s) {
+  if (!s) return fail(AKV_ERR_INVALID, "shape is NULL");
+  if (s->Hq <= 0 || s->Hkv <= 0 || s->Hq % s->Hkv)
+    return fail(AKV_ERR_INVALID, "need Hq %% Hkv == 0 (Hq=%d Hkv=%d)", s->Hq, s->Hkv);
+  if (s->dtype != AKV_F32 && s->dtype != AKV_BF16)
+    return fail(AKV_ERR_INVALID, "unknown dtype %d", (int)s->dtype);
+  if (!(s->rope_base > 1.0f) || !std::isfinite(s->rope_base))
+    return fail(AKV_ERR_INVALID, "rope_base must be finite and > 1");
+  if (s->D != kD) return fail(AKV_ERR_UNSUPPORTED, "head dim %d (only %d)", s->D, kD);
+  return AKV_OK;
+}
+
+// Validate one op log against the request's token count.
+akv_status check_oplog(const akv_oplog *o, int64_t T, int req) {
+  if (!o) return fail(AKV_ERR_INVALID, "request %d: op log is NULL", req);
+  if (o->n_msgs < 0 || o->n_drops < 0 || o->n_repos < 0)
+    return fail(AKV_ERR_INVALID, "request %d: negative count", req);
+  if (!o->msg_start) return fail(AKV_ERR_INVALID, "request %d: msg_start is NULL", req);
+  if (o->msg_start[0] != 0) return fail(AKV_ERR_INVALID, "request %d: msg_start[0] != 0", req);
+  for (int m = 0; m < o->n_msgs; ++m)
+    if (o->msg_start[m + 1] < o->msg_start[m])
+      return fail(AKV_ERR_INVALID, "request %d: msg_start decreases at %d", req, m);
+  if (T >= 0 && o->msg_start[o->n_msgs] != T)
+    return fail(AKV_ERR_INVALID, "request %d: messages hold %d tokens, rows %lld", req,
+                o->msg_start[o->n_msgs], (long long)T);
+  if (o->n_drops && (!o->drop_after || !o->drop_target))
+    return fail(AKV_ERR_INVALID, "request %d: drop arrays are NULL", req);
+  if (o->n_repos && !o->repos_after)
+    return fail(AKV_ERR_INVALID, "request %d: repos array is NULL", req);
+  for (int i = 0; i < o->n_drops; ++i) {
+    int a = o->drop_after[i], t = o->drop_target[i];
+    if (a < 0 || a >= o->n_msgs)
+      return fail(AKV_ERR_INVALID, "request %d: drop boundary %d out of range", req, a);
+    if (t < 0 || t > a)
+      return fail(AKV_ERR_INVALID,
+                  "request %d: drop target %d must be an appended message (<= %d)", req, t, a);
+  }
+  for (int i = 0; i < o->n_repos; ++i) {
+    int a = o->repos_after[i];
+    if (a < 0 || a >= o->n_msgs)
+      return fail(AKV_ERR_INVALID, "request %d: repos boundary %d out of range", req, a);
+  }
+  return AKV_OK;
+}
+
+}  // namespace
+
+void akv::rope_theta(float base, RopeTheta *out) {
+  for (int i = 0; i < kD / 2; ++i) out->th[i] = std::pow((double)base, -2.0 * i / kD);
+}
+
+// ------------------------------------------------------------------------
+// Plan
+// ------------------------------------------------------------------------
+
+struct WsLayout {
+  size_t status, tok_qpos, tok_seg, slot_src, slot_u, slot_dseg, slot_pos, qtiles, windows,
+      order, qr, kr, vp, total;
+};
+
+struct akv_plan {
+  akv_shape shape{};
+  int n_req = 0;
+  int64_t T = 0;
+  int max_ver = 1;
+  std::vector<int32_t> tok_pos, tok_seg, tok_ver, drop_seg;  // request-relative
+  std::vector<int32_t> slot_src, slot_u, slot_dseg, slot_pos;
+  std::vector<QTile> qtiles;
+  std::vector<uint32_t> windows;
+  std::vector<int32_t> order;
+  int64_t visible_pairs = 0, n_full = 0, n_segments = 0;
+  WsLayout ws{};
+};
+
+namespace {
+
+struct Group {  // run of permuted slots sharing one drop segment
+  int32_t begin, end, dseg;
+};
+
+// Plan one request: tables for rows [c0, c0+T) and its query tiles.
+void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
+  const int n = o->n_msgs;
+  const int32_t *ms = o->msg_start;
+  const int64_t T = ms[n];
+  std::vector<std::vector<int>> drops_at(n);
+  std::vector<char> repos_at(n, 0);
+  for (int i = 0; i < o->n_drops; ++i) drops_at[o->drop_after[i]].push_back(o->drop_target[i]);
+  for (int i = 0; i < o->n_repos; ++i) repos_at[o->repos_after[i]] = 1;
+
+  int32_t *tpos = P->tok_pos.data() + c0, *tseg = P->tok_seg.data() + c0;
+  int32_t *tver = P->tok_ver.data() + c0, *dseg = P->drop_seg.data() + c0;
+  std::vector<char> alive(n, 0);
+  std::vector<int32_t> msg_dseg(n, INT32_MAX);
+  // positions per version: version 0 and every repos
+  std::vector<std::vector<int32_t>> vpos(1, std::vector<int32_t>(T, -1));
+  std::vector<int> ver_first_msg(1, 0);  // first message appended in each version
+  int64_t next_pos = 0, n_active = 0;
+  int seg = 0, ver = 0;
+  for (int m = 0; m < n; ++m) {
+    const int64_t a = ms[m], b = ms[m + 1];
+    for (int64_t t = a; t < b; ++t) {
+      tpos[t] = (int32_t)next_pos;
+      vpos[ver][t] = (int32_t)next_pos;
+      ++next_pos;
+      tseg[t] = seg;
+      tver[t] = ver;
+      // row t sees the active cache at its start plus its own message prefix
+      P->visible_pairs += n_active + (t - a) + 1;
+    }
+    alive[m] = 1;
+    n_active += b - a;
+    bool op = false;
+    for (int j : drops_at[m]) {
+      op = true;
+      if (alive[j]) {
+        alive[j] = 0;
+        msg_dseg[j] = seg + 1;
+        n_active -= ms[j + 1] - ms[j];
+      }
+    }
+    if (repos_at[m]) {
+      op = true;
+      ++ver;
+      vpos.emplace_back(T, -1);
+      ver_first_msg.push_back(m + 1);
+      int32_t r = 0;
+      for (int j = 0; j <= m; ++j)
+        if (alive[j])
+          for (int64_t u = ms[j]; u < ms[j + 1]; ++u) vpos[ver][u] = r++;
+      next_pos = r;
+    }
+    if (op) ++seg;
+  }
+  const int n_seg = seg + 1, n_ver = ver + 1;
+  P->n_segments += n_seg;
+  for (int m = 0; m < n; ++m)
+    for (int64_t u = ms[m]; u < ms[m + 1]; ++u) dseg[u] = msg_dseg[m];
+
+  // permuted slot order: messages by decreasing drop segment, then logical order
+  std::vector<int> morder(n);
+  std::iota(morder.begin(), morder.end(), 0);
+  std::stable_sort(morder.begin(), morder.end(),
+                   [&](int x, int y) { return msg_dseg[x] > msg_dseg[y]; });
+  std::vector<Group> groups;
+  std::vector<int32_t> u_of(T);  // local slot -> local row
+  {
+    int64_t j = 0;
+    for (int m : morder) {
+      if (ms[m + 1] == ms[m]) continue;
+      if (groups.empty() || groups.back().dseg != msg_dseg[m])
+        groups.push_back({(int32_t)j, (int32_t)j, msg_dseg[m]});
+      for (int64_t u = ms[m]; u < ms[m + 1]; ++u) u_of[j++] = (int32_t)u;
+      groups.back().end = (int32_t)j;
+    }
+  }
+  for (int64_t j = 0; j < T; ++j) {
+    P->slot_src[c0 + j] = (int32_t)(c0 + u_of[j]);
+    P->slot_u[c0 + j] = (int32_t)(c0 + u_of[j]);
+    P->slot_dseg[c0 + j] = dseg[u_of[j]];
+    for (int v = 0; v < P->max_ver; ++v) {
+      int32_t p = v < n_ver ? vpos[v][u_of[j]] : -1;
+      P->slot_pos[(size_t)v * P->T + c0 + j] = p < 0 ? 0 : p;
+    }
+  }
+
+  // query tiles: per version, consecutive rows, 128 at a time
+  for (int v = 0; v < n_ver; ++v) {
+    int64_t r0 = ms[ver_first_msg[v]];
+    int64_t r1 = (v + 1 < n_ver) ? ms[ver_first_msg[v + 1]] : T;
+    for (int64_t t0 = r0; t0 < r1; t0 += kTileQ) {
+      const int64_t t1 = std::min<int64_t>(r1, t0 + kTileQ);
+      QTile q{};
+      q.t0 = (int32_t)(c0 + t0);
+      q.len = (int32_t)(t1 - t0);
+      q.ver = v;
+      q.req = req;
+      q.win_off = (int32_t)P->windows.size();
+      q.seg_lo = tseg[t0];
+      q.seg_hi = tseg[t1 - 1];
+      // visible slot intervals, in slot order: groups with dseg > seg_lo, the
+      // prefix of each with u <= t1-1
+      int64_t cover_end = -1;
+      for (const Group &g : groups) {
+        if (g.dseg <= q.seg_lo) break;  // groups are by decreasing dseg
+        if (u_of[g.begin] > t1 - 1) continue;
+        const int32_t *e = std::upper_bound(u_of.data() + g.begin, u_of.data() + g.end,
+                                            (int32_t)(t1 - 1));
+        int64_t a = g.begin, b = e - u_of.data();
+        if (a < cover_end) a = cover_end;
+        while (a < b) {
+          // full if every slot of [a, a+128) is in this request, in groups
+          // that outlive the tile, and not after the tile's first row
+          bool full = a + kTileK <= T;
+          if (full) {
+            int64_t s = a;
+            const Group *gp = &g;
+            while (full && s < a + kTileK) {
+              while (!(gp->begin <= s && s < gp->end)) ++gp;
+              int64_t last = std::min<int64_t>(gp->end, a + kTileK) - 1;
+              if (gp->dseg <= q.seg_hi || u_of[last] > t0) full = false;
+              s = last + 1;
+            }
+          }
+          P->windows.push_back((uint32_t)(c0 + a) | (full ? kWinFull : 0u));
+          if (full) ++P->n_full;
+          cover_end = a + kTileK;
+          a = cover_end;
+        }
+      }
+      q.win_cnt = (int32_t)(P->windows.size() - q.win_off);
+      P->qtiles.push_back(q);
+    }
+  }
+}
+
+void layout_workspace(akv_plan *P) {
+  WsLayout &w = P->ws;
+  const size_t T = (size_t)P->T, nt = P->qtiles.size(), nw = P->windows.size();
+  const size_t es = esize(P->shape.dtype);
+  size_t o = 0;
+  auto take = [&](size_t bytes, size_t al) {
+    o = align_up(o, al);
+    size_t r = o;
+    o += bytes;
+    return r;
+  };
+  w.status = take(256, 256);
+  w.tok_qpos = take(4 * T, 256);
+  w.tok_seg = take(4 * T, 256);
+  w.slot_src = take(4 * T, 256);
+  w.slot_u = take(4 * (T + kSlotPad), 256);
+  w.slot_dseg = take(4 * (T + kSlotPad), 256);
+  w.slot_pos = take(4 * T * P->max_ver, 256);
+  w.qtiles = take(sizeof(QTile) * nt, 256);
+  w.windows = take(4 * nw, 256);
+  w.order = take(4 * nt, 256);
+  w.qr = take(es * T * P->shape.Hq * kD, 1024);
+  w.kr = take(es * T * P->shape.Hkv * kD * P->max_ver, 1024);
+  w.vp = take(es * T * P->shape.Hkv * kD, 1024);
+  w.total = align_up(o, 1024);
+}
+
+PlanDev device_view(const akv_plan *P, void *ws) {
+  char *b = (char *)ws;
+  const WsLayout &w = P->ws;
+  PlanDev d{};
+  d.status = (uint32_t *)(b + w.status);
+  d.tok_qpos = (const int32_t *)(b + w.tok_qpos);
+  d.tok_seg = (const int32_t *)(b + w.tok_seg);
+  d.slot_src = (const int32_t *)(b + w.slot_src);
+  d.slot_u = (const int32_t *)(b + w.slot_u);
+  d.slot_dseg = (const int32_t *)(b + w.slot_dseg);
+  d.slot_pos = (const int32_t *)(b + w.slot_pos);
+  d.qtiles = (const QTile *)(b + w.qtiles);
+  d.windows = (const uint32_t *)(b + w.windows);
+  d.order = (const int32_t *)(b + w.order);
+  d.qr = b + w.qr;
+  d.kr = b + w.kr;
+  d.vp = b + w.vp;
+  d.T = P->T;
+  d.n_qtiles = (int32_t)P->qtiles.size();
+  d.max_ver = P->max_ver;
+  d.Hq = P->shape.Hq;
+  d.Hkv = P->shape.Hkv;
+  d.rope_base = P->shape.rope_base;
+  d.dtype = (int32_t)P->shape.dtype;
+  return d;
+}
+
+akv_status upload_plan(const akv_plan *P, void *ws, cudaStream_t s) {
+  char *b = (char *)ws;
+  const WsLayout &w = P->ws;
+  struct Part {
+    size_t off;
+    const void *src;
+    size_t bytes;
+  } parts[] = {
+      {w.tok_qpos, P->tok_pos.data(), 4 * P->tok_pos.size()},
+      {w.tok_seg, P->tok_seg.data(), 4 * P->tok_seg.size()},
+      {w.slot_src, P->slot_src.data(), 4 * P->slot_src.size()},
+      {w.slot_u, P->slot_u.data(), 4 * P->slot_u.size()},
+      {w.slot_dseg, P->slot_dseg.data(), 4 * P->slot_dseg.size()},
+      {w.slot_pos, P->slot_pos.data(), 4 * P->slot_pos.size()},
+      {w.qtiles, P->qtiles.data(), sizeof(QTile) * P->qtiles.size()},
+      {w.windows, P->windows.data(), 4 * P->windows.size()},
+      {w.order, P->order.data(), 4 * P->order.size()},
+  };
+  cudaError_t e = cudaMemsetAsync(b + w.status, 0, 256, s);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  for (const Part &p : parts) {
+    if (!p.bytes) continue;
+    e = cudaMemcpyAsync(b + p.off, p.src, p.bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+  }
+  return AKV_OK;
+}
+
+akv_status check_ws(const akv_plan *P, void *ws, size_t bytes) {
+  if (!ws && P->ws.total) return fail(AKV_ERR_WORKSPACE, "workspace is NULL");
+  if ((uintptr_t)ws % 256) return fail(AKV_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  if (bytes < P->ws.total)
+    return fail(AKV_ERR_WORKSPACE, "workspace %zu bytes, need %zu", bytes, P->ws.total);
+  return AKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *akv_last_error(void) { return g_err.c_str(); }
+
+const char *akv_version(void) { return "akv-gb300 0.1 (sm_103a)"; }
+
+akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                           const int32_t *logical_idx, const akv_oplog *ops,
+                           akv_plan **plan_out) {
+  if (akv_status f = injected_fault("akv_plan_create")) return f;
+  if (!plan_out) return fail(AKV_ERR_INVALID, "plan_out is NULL");
+  *plan_out = nullptr;
+  if (akv_status st = check_shape(shape)) return st;
+  if (n_req < 0 || (n_req > 0 && (!cu_seqlens || !ops)))
+    return fail(AKV_ERR_INVALID, "bad request batch");
+  if (n_req > 0 && cu_seqlens[0] != 0) return fail(AKV_ERR_INVALID, "cu_seqlens[0] != 0");
+  for (int b = 0; b < n_req; ++b) {
+    if (cu_seqlens[b + 1] < cu_seqlens[b])
+      return fail(AKV_ERR_INVALID, "cu_seqlens decreases at %d", b);
+    if (akv_status st = check_oplog(&ops[b], cu_seqlens[b + 1] - cu_seqlens[b], b)) return st;
+  }
+  const int64_t T = n_req ? cu_seqlens[n_req] : 0;
+  if (T >= (int64_t)INT32_MAX - kSlotPad) return fail(AKV_ERR_UNSUPPORTED, "too many rows");
+  if (logical_idx)
+    for (int b = 0; b < n_req; ++b)
+      for (int64_t i = cu_seqlens[b]; i < cu_seqlens[b + 1]; ++i)
+        if (logical_idx[i] != i - cu_seqlens[b])
+          return fail(AKV_ERR_INVALID, "row %lld carries logical index %d, expected %lld",
+                      (long long)i, logical_idx[i], (long long)(i - cu_seqlens[b]));
+  akv_plan *P = new (std::nothrow) akv_plan;
+  if (!P) return fail(AKV_ERR_INVALID, "host allocation failed");
+  P->shape = *shape;
+  P->n_req = n_req;
+  P->T = T;
+  int max_ver = 1;
+  for (int b = 0; b < n_req; ++b) {
+    std::vector<int> rb(ops[b].repos_after, ops[b].repos_after + ops[b].n_repos);
+    std::sort(rb.begin(), rb.end());
+    max_ver = std::max<int>(max_ver, 1 + (int)(std::unique(rb.begin(), rb.end()) - rb.begin()));
+  }
+  P->max_ver = max_ver;
+  try {
+    P->tok_pos.assign(T, 0);
+    P->tok_seg.assign(T, 0);
+    P->tok_ver.assign(T, 0);
+    P->drop_seg.assign(T, INT32_MAX);
+    P->slot_src.assign(T, 0);
+    P->slot_u.assign(T + kSlotPad, INT32_MAX);
+    P->slot_dseg.assign(T + kSlotPad, INT32_MIN);
+    P->slot_pos.assign((size_t)T * max_ver, 0);
+    for (int b = 0; b < n_req; ++b) plan_request(P, b, cu_seqlens[b], &ops[b]);
+    P->order.resize(P->qtiles.size());
+    std::iota(P->order.begin(), P->order.end(), 0);
+    std::stable_sort(P->order.begin(), P->order.end(), [&](int x, int y) {
+      return P->qtiles[x].win_cnt > P->qtiles[y].win_cnt;
+    });
+  } catch (const std::bad_alloc &) {
+    delete P;
+    return fail(AKV_ERR_INVALID, "host allocation failed while planning");
+  }
+  layout_workspace(P);
+  *plan_out = P;
+  return AKV_OK;
+}
+
+void akv_plan_destroy(akv_plan *plan) { delete plan; }
+
+akv_status akv_plan_get_info(const akv_plan *P, akv_plan_info *info) {
+  if (!P || !info) return fail(AKV_ERR_INVALID, "NULL argument");
+  info->T = P->T;
+  info->n_qtiles = (int64_t)P->qtiles.size();
+  info->n_windows = (int64_t)P->windows.size();
+  info->n_full_windows = P->n_full;
+  info->visible_pairs = P->visible_pairs;
+  info->n_segments = P->n_segments;
+  info->max_versions = P->max_ver;
+  info->reserved = 0;
+  info->workspace_bytes = P->ws.total;
+  return AKV_OK;
+}
+
+akv_status akv_plan_tables(const akv_plan *P, int32_t *tok_pos, int32_t *tok_seg,
+                           int32_t *tok_ver, int32_t *drop_seg) {
+  if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
+  const size_t n = (size_t)P->T * 4;
+  if (tok_pos) memcpy(tok_pos, P->tok_pos.data(), n);
+  if (tok_seg) memcpy(tok_seg, P->tok_seg.data(), n);
+  if (tok_ver) memcpy(tok_ver, P->tok_ver.data(), n);
+  if (drop_seg) memcpy(drop_seg, P->drop_seg.data(), n);
+  return AKV_OK;
+}
+
+namespace {
+akv_status check_run(const akv_plan *P, void *workspace, size_t workspace_bytes) {
+  if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
+  if (P->shape.dtype == AKV_BF16 && (P->shape.Hq / P->shape.Hkv) % 2)
+    return fail(AKV_ERR_UNSUPPORTED,
+                "bf16 prefill needs an even number of query heads per KV head");
+  return check_ws(P, workspace, workspace_bytes);
+}
+}  // namespace
+
+akv_status akv_segment_prepare(const akv_plan *P, const void *q, const void *k, const void *v,
+                               void *workspace, size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_segment_prepare")) return f;
+  if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
+  if (P->T == 0) return AKV_OK;
+  if (!q || !k || !v) return fail(AKV_ERR_INVALID, "NULL tensor");
+  if (akv_status st = check_run(P, workspace, workspace_bytes)) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (akv_status st = upload_plan(P, workspace, s)) return st;
+  RopeTheta th;
+  rope_theta(P->shape.rope_base, &th);
+  cudaError_t e = launch_prep(device_view(P, workspace), q, k, v, th, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rope/permute pre-pass");
+  return AKV_OK;
+}
+
+akv_status akv_segment_attend(const akv_plan *P, void *out, void *workspace,
+                              size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_segment_attend")) return f;
+  if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
+  if (P->T == 0) return AKV_OK;
+  if (!out) return fail(AKV_ERR_INVALID, "NULL output");
+  if (akv_status st = check_run(P, workspace, workspace_bytes)) return st;
+  PlanDev d = device_view(P, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = P->shape.dtype == AKV_F32 ? launch_attn_simt_f32(d, out, s)
+                                            : launch_attn_tc_bf16(d, out, s);
+  if (e != cudaSuccess) return cuda_fail(e, "segment attention");
+  return AKV_OK;
+}
+
+akv_status akv_segment_attention_run(const akv_plan *P, const void *q, const void *k,
+                                     const void *v, void *out, void *workspace,
+                                     size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_segment_attention_run")) return f;
+  if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
+  if (P->T == 0) return AKV_OK;
+  if (!q || !k || !v || !out) return fail(AKV_ERR_INVALID, "NULL tensor");
+  if (akv_status st = check_run(P, workspace, workspace_bytes)) return st;
+  if (akv_status st = akv_segment_prepare(P, q, k, v, workspace, workspace_bytes, stream))
+    return st;
+  return akv_segment_attend(P, out, workspace, workspace_bytes, stream);
+}
+
+size_t akv_segment_attention_workspace(const akv_shape *shape, int32_t n_req,
+                                       const int32_t *cu_seqlens, const akv_oplog *ops) {
+  akv_plan *P = nullptr;
+  if (akv_plan_create(shape, n_req, cu_seqlens, nullptr, ops, &P) != AKV_OK) return 0;
+  size_t r = P->ws.total;
+  akv_plan_destroy(P);
+  return r;
+}
+
+akv_status akv_segment_attention(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                                 const int32_t *logical_idx, const akv_oplog *ops, const void *q,
+                                 const void *k, const void *v, void *out, void *workspace,
+                                 size_t workspace_bytes, akv_stream_t stream) {
+  akv_plan *P = nullptr;
+  akv_status st = akv_plan_create(shape, n_req, cu_seqlens, logical_idx, ops, &P);
+  if (st != AKV_OK) return st;
+  st = akv_segment_attention_run(P, q, k, v, out, workspace, workspace_bytes, stream);
+  akv_plan_destroy(P);
+  return st;
+}
+
+akv_status akv_segment_visible_counts(const akv_plan *P, int32_t *counts, void *workspace,
+                                      size_t workspace_bytes, akv_stream_t stream) {
+  if (!P || !counts) return fail(AKV_ERR_INVALID, "NULL argument");
+  if (P->T == 0) return AKV_OK;
+  if (akv_status st = check_ws(P, workspace, workspace_bytes)) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (akv_status st = upload_plan(P, workspace, s)) return st;
+  cudaError_t e = launch_visible_counts(device_view(P, workspace), counts, s);
+  if (e != cudaSuccess) return cuda_fail(e, "visible counts");
+  return AKV_OK;
+}
+
+akv_status akv_workspace_status(void *workspace, akv_stream_t stream, uint32_t *code) {
+  if (!workspace || !code) return fail(AKV_ERR_INVALID, "NULL argument");
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, 4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *code = h;
+  if (h) return fail(AKV_ERR_DEVICE, "kernel status word 0x%x", h);
+  return AKV_OK;
+}
+
+// ------------------------------------------------------------------------
+// Compaction
+// ------------------------------------------------------------------------
+
+namespace {
+struct CompactHost {
+  int32_t upto, n_msgs, T_upto, br_end, r, has_br;
+  std::vector<uint8_t> keep, alive_br;
+  int64_t n_active;
+};
+
+akv_status compact_host(const akv_oplog *o, int32_t upto, CompactHost *c) {
+  const int n = o->n_msgs;
+  if (upto < 0) upto = n - 1;
+  if (n == 0) {
+    c->upto = -1;
+    c->n_msgs = 0;
+    c->T_upto = 0;
+    c->br_end = 0;
+    c->r = 0;
+    c->has_br = 0;
+    c->n_active = 0;
+    return AKV_OK;
+  }
+  if (upto >= n) return fail(AKV_ERR_INVALID, "boundary %d out of range", upto);
+  c->upto = upto;
+  c->n_msgs = upto + 1;
+  c->T_upto = o->msg_start[upto + 1];
+  // first drop boundary of each message, and repos boundaries before upto
+  std::vector<int> first_drop(n, INT32_MAX);
+  for (int i = 0; i < o->n_drops; ++i)
+    first_drop[o->drop_target[i]] = std::min(first_drop[o->drop_target[i]], o->drop_after[i]);
+  int br = -1;
+  for (int i = 0; i < o->n_repos; ++i)
+    if (o->repos_after[i] < upto) br = std::max(br, o->repos_after[i]);
+  c->keep.assign(upto + 1, 0);
+  c->alive_br.assign(upto + 1, 0);
+  c->n_active = 0;
+  c->r = 0;
+  for (int m = 0; m <= upto; ++m) {
+    c->keep[m] = first_drop[m] > upto;
+    if (c->keep[m]) c->n_active += o->msg_start[m + 1] - o->msg_start[m];
+    if (br >= 0 && m <= br) {
+      c->alive_br[m] = first_drop[m] > br;
+      if (c->alive_br[m]) c->r += o->msg_start[m + 1] - o->msg_start[m];
+    }
+  }
+  c->has_br = br >= 0;
+  c->br_end = br >= 0 ? o->msg_start[br + 1] : 0;
+  return AKV_OK;
+}
+
+size_t compact_ws_bytes(int n_msgs, int T) {
+  return align_up(4 * (size_t)(n_msgs + 1), 256) + 2 * align_up((size_t)n_msgs + 1, 256) +
+         align_up(8 * (size_t)compact_blocks(T), 256);
+}
+}  // namespace
+
+size_t akv_compact_workspace(const akv_oplog *ops, int32_t T) {
+  if (!ops || ops->n_msgs < 0) return 0;
+  return compact_ws_bytes(ops->n_msgs, T);
+}
+
+akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *active_idx,
+                       int32_t *active_pos, int32_t *n_active, void *workspace,
+                       size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_compact")) return f;
+  if (akv_status st = check_oplog(ops, T, 0)) return st;
+  if (!n_active || !active_idx || !active_pos) return fail(AKV_ERR_INVALID, "NULL output");
+  CompactHost c;
+  if (akv_status st = compact_host(ops, upto, &c)) return st;
+  *n_active = (int32_t)c.n_active;
+  if (c.T_upto == 0) return AKV_OK;
+  const size_t need = compact_ws_bytes(ops->n_msgs, T);
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
+    return fail(AKV_ERR_WORKSPACE, "compact workspace: need %zu aligned bytes", need);
+  cudaStream_t s = (cudaStream_t)stream;
+  char *b = (char *)workspace;
+  size_t o0 = 0, o1 = align_up(4 * (size_t)(ops->n_msgs + 1), 256);
+  size_t o2 = o1 + align_up((size_t)ops->n_msgs + 1, 256);
+  size_t o3 = o2 + align_up((size_t)ops->n_msgs + 1, 256);
+  cudaError_t e = cudaMemcpyAsync(b + o0, ops->msg_start, 4 * (size_t)(c.n_msgs + 1),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + o1, c.keep.data(), c.n_msgs, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + o2, c.alive_br.data(), c.n_msgs, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "compact upload");
+  CompactDev d{};
+  d.msg_start = (const int32_t *)(b + o0);
+  d.keep = (const uint8_t *)(b + o1);
+  d.alive_br = (const uint8_t *)(b + o2);
+  d.block_cnt = (int32_t *)(b + o3);
+  d.n_msgs = c.n_msgs;
+  d.T = c.T_upto;
+  d.br_end = c.br_end;
+  d.r = c.r;
+  d.has_br = c.has_br;
+  e = launch_compact(d, active_idx, active_pos, s);
+  if (e != cudaSuccess) return cuda_fail(e, "compact");
+  return AKV_OK;
+}
+
+// ------------------------------------------------------------------------
+// Repos rotate, append, decode
+// ------------------------------------------------------------------------
+
+akv_status akv_repos_rotate(const akv_shape *shape, int32_t r, const int32_t *src_idx,
+                            const int32_t *pos_from, const int32_t *pos_to, const void *k_in,
+                            const void *v_in, void *k_out, void *v_out, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_repos_rotate")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (r < 0) return fail(AKV_ERR_INVALID, "r < 0");
+  if (r == 0) return AKV_OK;
+  if (!src_idx || !pos_from || !k_in || !v_in || !k_out || !v_out)
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_repos(shape->dtype, shape->Hkv, r, src_idx, pos_from, pos_to, k_in, v_in,
+                               k_out, v_out, th, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "repos rotate");
+  return AKV_OK;
+}
+
+akv_status akv_append_kv(const akv_shape *shape, int32_t n, const void *k_new, const void *v_new,
+                         const int32_t *pos, const int32_t *slot, void *k_pool, void *v_pool,
+                         akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_append_kv")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (n < 0) return fail(AKV_ERR_INVALID, "n < 0");
+  if (n == 0) return AKV_OK;
+  if (!k_new || !v_new || !pos || !slot || !k_pool || !v_pool)
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_append(shape->dtype, shape->Hkv, n, k_new, v_new, pos, slot, k_pool,
+                                v_pool, th, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "append");
+  return AKV_OK;
+}
+
+size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv) {
+  if (!shape || B < 0 || max_kv < 0 || shape->Hkv <= 0 || shape->Hq % shape->Hkv) return 0;
+  return decode_partials_bytes(B, shape->Hq, max_kv);
+}
+
+akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
+                                const int32_t *q_pos, const void *k_pool, const void *v_pool,
+                                const int32_t *kv_indptr, const int32_t *kv_indices,
+                                int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
+                                akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_decode_attention")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B == 0) return AKV_OK;
+  if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out || (max_kv > 0 && !kv_indices))
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
+  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv);
+  if (need && (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need))
+    return fail(AKV_ERR_WORKSPACE, "decode workspace: need %zu aligned bytes", need);
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_decode(shape->dtype, B, shape->Hq, shape->Hkv, q, q_pos, k_pool, v_pool,
+                                kv_indptr, kv_indices, max_kv, out, workspace, th,
+                                (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode");
+  return AKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// Device helpers shared by the CUDA translation units of libakv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "akv_internal.h"
+
+namespace akv {
+
+// cos/sin of pos * theta.  The angle is formed and reduced modulo 2*pi in
+// double (one product, one fused multiply-add: exact enough for positions up
+// to 2^31), then evaluated in float on an argument in [-pi, pi].
+__device__ __forceinline__ void rope_cs(double theta, double pos, float *c, float *s) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const double a = pos * theta;
+  const double k = rint(a * (1.0 / two_pi));
+  const float r = (float)fma(-k, two_pi, a);
+  sincosf(r, s, c);
+}
+
+// 16-byte chunks of one head row (D = 64): a bf16 chunk holds 8 elements, an
+// f32 chunk 4.  Pair (i, i + D/2) lives in chunks c and c + kHalfChunks.
+template <typename T>
+struct Chunk;
+template <>
+struct Chunk<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+};
+template <>
+struct Chunk<__half> {
+  static constexpr int kElems = 8;
+};
+template <>
+struct Chunk<float> {
+  static constexpr int kElems = 4;
+};
+
+template <typename T>
+__device__ __forceinline__ void chunk_to_f32(const uint4 &u, float *f);
+template <>
+__device__ __forceinline__ void chunk_to_f32<__nv_bfloat16>(const uint4 &u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void chunk_to_f32<float>(const uint4 &u, float *f) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 f32_to_chunk(const float *f);
+template <>
+__device__ __forceinline__ uint4 f32_to_chunk<__nv_bfloat16>(const float *f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ uint4 f32_to_chunk<__half>(const float *f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ uint4 f32_to_chunk<float>(const float *f) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+
+// Rotate chunk pair c / c + half of one head row: y = R(angle) x with
+// per-frequency cos/sin cs[i], sn[i] (i = frequency index within the half).
+// Tin is read, Tout written (same number of elements per 16-byte chunk).
+// Returns true if an output does not fit an fp16 operand (|y| > 65504).
+template <typename Tin, typename Tout = Tin>
+__device__ __forceinline__ bool rotate_pair(const Tin *src, Tout *dst, int c, const float *cs,
+                                            const float *sn) {
+  constexpr int E = Chunk<Tin>::kElems;
+  static_assert(E == Chunk<Tout>::kElems, "chunk shapes differ");
+  constexpr int H = (kD / 2) / E;  // chunks per half row
+  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+  const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + c + H);
+  float x1[E], x2[E], y1[E], y2[E];
+  chunk_to_f32<Tin>(a, x1);
+  chunk_to_f32<Tin>(b, x2);
+  float big = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float co = cs[c * E + e], si = sn[c * E + e];
+    y1[e] = x1[e] * co - x2[e] * si;
+    y2[e] = x1[e] * si + x2[e] * co;
+    big = fmaxf(big, fmaxf(fabsf(y1[e]), fabsf(y2[e])));
+  }
+  reinterpret_cast<uint4 *>(dst)[c] = f32_to_chunk<Tout>(y1);
+  reinterpret_cast<uint4 *>(dst)[c + H] = f32_to_chunk<Tout>(y2);
+  return !(big <= 65504.f);
+}
+
+}  // namespace akv

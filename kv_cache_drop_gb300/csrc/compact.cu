@@ -1,0 +1,137 @@
+// Compaction of the active cache (drop, paper review page section 3.3; the
+// active cache vs the logical trajectory, explainer page section 1).
+//
+// The host reduces the op log to two flags per message (survives the drops
+// up to the boundary; alive right after the last earlier repos).  On the
+// device every token takes its message's flags, and two exclusive scans give
+// each survivor its place in the compacted list and its position (rank among
+// the survivors of the last repos, or r + offset for later appends).  Two
+// launches: per-block counts, then per-block prefix (over the few preceding
+// block counts) + block scan + scatter.  Bit-exact integer work.
+#include "common.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kPer = 8;  // consecutive tokens per thread
+constexpr int kBlock = kThreads * kPer;
+
+__device__ __forceinline__ int msg_of(const int32_t *ms, int n_msgs, int u) {
+  int lo = 0, hi = n_msgs;  // ms[lo] <= u < ms[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ms + mid) <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// flags of the kPer tokens of this thread: bit i of keep / alive
+__device__ __forceinline__ void token_flags(const CompactDev &c, int u0, uint32_t *keep,
+                                            uint32_t *alive) {
+  *keep = 0;
+  *alive = 0;
+  if (u0 >= c.T) return;
+  int m = msg_of(c.msg_start, c.n_msgs, u0);
+  for (int i = 0; i < kPer; ++i) {
+    const int u = u0 + i;
+    if (u >= c.T) break;
+    while (__ldg(c.msg_start + m + 1) <= u) ++m;
+    if (c.keep[m]) *keep |= 1u << i;
+    if (c.has_br && u < c.br_end && c.alive_br[m]) *alive |= 1u << i;
+  }
+}
+
+// exclusive block scan of two counters packed as (hi << 16) | lo
+__device__ __forceinline__ uint32_t block_exscan(uint32_t x, uint32_t *total) {
+  __shared__ uint32_t warp_sum[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_sum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sum[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const uint32_t before = (warp ? warp_sum[warp - 1] : 0u) + inc - x;
+  *total = warp_sum[kThreads / 32 - 1];
+  return before;
+}
+
+__global__ void __launch_bounds__(kThreads) compact_count_kernel(CompactDev c) {
+  uint32_t keep, alive;
+  token_flags(c, blockIdx.x * kBlock + threadIdx.x * kPer, &keep, &alive);
+  uint32_t total;
+  block_exscan(((uint32_t)__popc(alive) << 16) | (uint32_t)__popc(keep), &total);
+  if (threadIdx.x == 0) {
+    c.block_cnt[2 * blockIdx.x] = (int32_t)(total & 0xffffu);
+    c.block_cnt[2 * blockIdx.x + 1] = (int32_t)(total >> 16);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev c, int32_t *active_idx,
+                                                                 int32_t *active_pos) {
+  __shared__ int32_t base_keep, base_alive;
+  if (threadIdx.x < 32) {
+    int32_t a = 0, b = 0;
+    for (int i = threadIdx.x; i < (int)blockIdx.x; i += 32) {
+      a += c.block_cnt[2 * i];
+      b += c.block_cnt[2 * i + 1];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if (threadIdx.x == 0) {
+      base_keep = a;
+      base_alive = b;
+    }
+  }
+  const int u0 = blockIdx.x * kBlock + threadIdx.x * kPer;
+  uint32_t keep, alive;
+  token_flags(c, u0, &keep, &alive);
+  uint32_t total;
+  const uint32_t ex = block_exscan(((uint32_t)__popc(alive) << 16) | (uint32_t)__popc(keep), &total);
+  int32_t k_at = base_keep + (int32_t)(ex & 0xffffu);
+  int32_t a_at = base_alive + (int32_t)(ex >> 16);
+  for (int i = 0; i < kPer; ++i) {
+    const int u = u0 + i;
+    if (u >= c.T) break;
+    int32_t pos;
+    if (!c.has_br) pos = u;
+    else if (u < c.br_end) pos = a_at;
+    else pos = c.r + (u - c.br_end);
+    if (alive >> i & 1u) ++a_at;
+    if (keep >> i & 1u) {
+      active_idx[k_at] = u;
+      active_pos[k_at] = pos;
+      ++k_at;
+    }
+  }
+}
+
+}  // namespace
+
+int compact_blocks(int T) { return (T + kBlock - 1) / kBlock; }
+
+cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *active_pos,
+                           cudaStream_t s) {
+  const int nb = compact_blocks(c.T);
+  compact_count_kernel<<<nb, kThreads, 0, s>>>(c);
+  compact_write_kernel<<<nb, kThreads, 0, s>>>(c, active_idx, active_pos);
+  return cudaGetLastError();
+}
+
+}  // namespace akv

@@ -1,0 +1,445 @@
+// Decode attention over the active cache in a page-size-1 pool (paper review
+// page section 4 serving flow: decode reads only the active cache; system
+// README: drop/repos work at page size 1).
+//
+// Split-KV: request b's index list is cut into chunks of kChunk keys; one CTA
+// takes (chunk, KV head g, request b) and produces a partial (row max m, row
+// sum l, unnormalised output o) for the Hq/Hkv query heads of group g; a
+// combine kernel merges the partials by their log-sum-exp.
+//
+// bf16: the group's query heads form the rows of an m16n8k16 tensor-core tile
+// (S = Q K^T with K rows as the B operand, then O += P V with P reused from
+// the S accumulator registers); keys and values are gathered 16 rows at a
+// time with 16-byte cp.async into an XOR-swizzled shared tile, several tiles
+// in flight per warp.  The work is bound by the gather from HBM (2 x 128 B
+// per key and head group); the tensor-core tile only keeps the arithmetic
+// off the critical path.
+// fp32: one thread per key, FMA dot products, block-level merge.
+#include "common.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kChunk = 2048;  // keys per CTA
+constexpr int kWarps = 4;
+constexpr int kTileKeys = 16;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Partials {
+  float *ml;  // [B][Hq][ns][2]  (m in log2 units, l)
+  float *o;   // [B][Hq][ns][kD]
+};
+
+__host__ __device__ inline int n_splits(int max_kv) { return max_kv <= 0 ? 1 : (max_kv + kChunk - 1) / kChunk; }
+
+Partials partials(void *ws, int B, int Hq, int max_kv) {
+  const int ns = n_splits(max_kv);
+  Partials p;
+  p.ml = (float *)ws;
+  const size_t ml_bytes = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
+  p.o = (float *)((char *)ws + ml_bytes);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+  const int n = valid ? 16 : 0;  // 0 source bytes: zero fill
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
+                                        uint32_t &d) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
+                                          uint32_t &d) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// byte offset of (row, 16-byte chunk) in a [16][64] bf16 tile, XOR swizzled
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
+                       const int32_t *__restrict__ qpos, const __nv_bfloat16 *__restrict__ kp,
+                       const __nv_bfloat16 *__restrict__ vp, const int32_t *__restrict__ indptr,
+                       const int32_t *__restrict__ indices, Partials part, RopeTheta th) {
+  // dynamic smem: per warp kStages x (K tile 2 KiB + V tile 2 KiB); reused
+  // for the merge of the warps' partials
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float cs[kD / 2], sn[kD / 2];
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int ns = gridDim.x;
+  const int grp = Hq / Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int beg = indptr[b], n = indptr[b + 1] - beg;
+  const int c0 = split * kChunk, c1 = min(n, c0 + kChunk);
+  if (c0 >= n) return;  // the combine reads only the splits that hold keys
+
+  if (threadIdx.x < kD / 2) rope_cs(th.th[threadIdx.x], (double)qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
+  __syncthreads();
+
+  // Q fragments (A operand, rows = query heads of the group, 16 rows padded
+  // with zeros), rotated at the query position; 1/sqrt(D) * log2(e) folded in.
+  uint32_t qa[4][4];
+  {
+    const float qs = 0.125f * kLog2e;
+    float qv[2][16];  // [row half][element]: rows gid and gid+8
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = gid + 8 * hh;
+      const bool ok = row < grp;
+      const __nv_bfloat16 *qrow = q + ((int64_t)b * Hq + g * grp + (ok ? row : 0)) * kD;
+      // elements held by this thread: ks*16 + {2tig, 2tig+1, 2tig+8, 2tig+9}
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          qv[hh][ks * 4 + e] = ok ? __bfloat162float(qrow[d]) : 0.f;
+        }
+    }
+    // rotate: element d (< 32) pairs with d + 32, i.e. k-step ks with ks + 2
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          const float x1 = qv[hh][ks * 4 + e], x2 = qv[hh][(ks + 2) * 4 + e];
+          qv[hh][ks * 4 + e] = (x1 * cs[d] - x2 * sn[d]) * qs;
+          qv[hh][(ks + 2) * 4 + e] = (x1 * sn[d] + x2 * cs[d]) * qs;
+        }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks][0] = pack_bf16(qv[0][ks * 4 + 0], qv[0][ks * 4 + 1]);
+      qa[ks][1] = pack_bf16(qv[1][ks * 4 + 0], qv[1][ks * 4 + 1]);
+      qa[ks][2] = pack_bf16(qv[0][ks * 4 + 2], qv[0][ks * 4 + 3]);
+      qa[ks][3] = pack_bf16(qv[1][ks * 4 + 2], qv[1][ks * 4 + 3]);
+    }
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  uint8_t *wsm = smem + warp * kStages * 4096;
+  const uint32_t wsm_u = smem_u32(wsm);
+  const int n_tiles = c0 < c1 ? (c1 - c0 + kTileKeys - 1) / kTileKeys : 0;
+  // tiles of this warp: warp, warp + kWarps, ...
+  auto issue = [&](int it) {
+    const int tile = warp + it * kWarps;
+    const int stage = it % kStages;
+    if (tile < n_tiles) {
+      const int k0 = c0 + tile * kTileKeys;
+      int slot = 0;
+      const bool have = lane < kTileKeys && k0 + lane < c1;
+      if (have) slot = __ldg(indices + beg + k0 + lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = lane + 32 * i;  // 128 chunks per tile: key = idx/8, chunk = idx%8
+        const int key = idx >> 3, ch = idx & 7;
+        const int s = __shfl_sync(0xffffffffu, slot, key);
+        const bool valid = k0 + key < c1;
+        const int64_t off = ((int64_t)s * Hkv + g) * kD + ch * 8;
+        cp_async16(wsm_u + stage * 4096 + swz(key, ch), kp + off, valid);
+        cp_async16(wsm_u + stage * 4096 + 2048 + swz(key, ch), vp + off, valid);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
+  };
+
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+#pragma unroll
+  for (int it = 0; it < kStages - 1; ++it) issue(it);
+  for (int it = 0; it < my_tiles; ++it) {
+    issue(it + kStages - 1);
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kStages - 1));
+    __syncwarp();
+    const uint32_t kt = wsm_u + (it % kStages) * 4096, vt = kt + 2048;
+    const int k0 = c0 + (warp + it * kWarps) * kTileKeys;
+    // S = Q K^T: two n-blocks of 8 keys
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      // matrices: (keys 0-7, d lo), (keys 0-7, d hi), (keys 8-15, d lo), (keys 8-15, d hi)
+      const int mi = lane >> 3;
+      const int key = (mi >> 1) * 8 + (lane & 7);
+      const int ch = ks * 2 + (mi & 1);
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(kt + swz(key, ch), b00, b01, b10, b11);
+      mma_bf16(s[0], qa[ks], b00, b01);
+      mma_bf16(s[1], qa[ks], b10, b11);
+    }
+    // mask the ragged tail; online softmax in log2 units
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = k0 + nb * 8 + 2 * tig + (e & 1);
+        if (key >= c1) s[nb][e] = -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+      }
+    float alpha[2], mref[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mn = fmaxf(m[r], mx[r]);
+      mref[r] = mn == -INFINITY ? 0.f : mn;
+      alpha[r] = exp2f(m[r] - mref[r]);
+      m[r] = mn;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nb][e] = exp2f(s[nb][e] - mref[e >> 1]);
+        rs[e >> 1] += s[nb][e];
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + rs[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    // O += P V: P from the S accumulators (keys as k), V through ldmatrix.trans
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int nb2 = 0; nb2 < 4; ++nb2) {
+      // matrices: (keys 0-7, d 16nb2..+7), (keys 8-15, same), (keys 0-7, d +8), (keys 8-15, d +8)
+      const int mi = lane >> 3;
+      const int key = (mi & 1) * 8 + (lane & 7);
+      const int ch = nb2 * 2 + (mi >> 1);
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vt + swz(key, ch), v0, v1, v2, v3);
+      mma_bf16(o[2 * nb2], pa, v0, v1);
+      mma_bf16(o[2 * nb2 + 1], pa, v2, v3);
+    }
+    __syncwarp();
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::);
+  __syncthreads();
+
+  // row sums over the quad
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  // merge the warps: smem [warp][16 rows][kD] + m, l
+  float *mo = reinterpret_cast<float *>(smem);           // kWarps*16*64 floats = 16 KiB
+  float *mm = mo + kWarps * 16 * kD;                      // kWarps*16
+  float *ml = mm + kWarps * 16;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = gid + 8 * (e >> 1), col = i * 8 + 2 * tig + (e & 1);
+      mo[(warp * 16 + row) * kD + col] = o[i][e];
+    }
+  if (tig == 0) {
+    mm[warp * 16 + gid] = m[0];
+    mm[warp * 16 + gid + 8] = m[1];
+    ml[warp * 16 + gid] = l[0];
+    ml[warp * 16 + gid + 8] = l[1];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < grp * kD; idx += kWarps * 32) {
+    const int row = idx / kD, col = idx % kD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * 16 + row]);
+    const float Mr = M == -INFINITY ? 0.f : M;
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = exp2f(mm[w * 16 + row] - Mr);
+      L += ml[w * 16 + row] * f;
+      acc += mo[(w * 16 + row) * kD + col] * f;
+    }
+    const int h = g * grp + row;
+    const int64_t pi = ((int64_t)b * Hq + h) * ns + split;
+    part.o[pi * kD + col] = acc;
+    if (col == 0) {
+      part.ml[2 * pi] = M;
+      part.ml[2 * pi + 1] = L;
+    }
+  }
+}
+
+// fp32: thread per key, block of 128 threads per (split, query head, request)
+__global__ void __launch_bounds__(128)
+    decode_f32_kernel(int Hq, int Hkv, const float *__restrict__ q, const int32_t *__restrict__ qpos,
+                      const float *__restrict__ kp, const float *__restrict__ vp,
+                      const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                      Partials part, RopeTheta th) {
+  __shared__ float qs[kD];
+  __shared__ float red_m[4], red_l[4];
+  __shared__ float red_o[4][kD];
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int ns = gridDim.x, g = h / (Hq / Hkv);
+  const int beg = indptr[b], n = indptr[b + 1] - beg;
+  const int c0 = split * kChunk, c1 = min(n, c0 + kChunk);
+  if (c0 >= n) return;
+  if (threadIdx.x < kD / 2) {
+    float c, s;
+    rope_cs(th.th[threadIdx.x], (double)qpos[b], &c, &s);
+    const float *qr = q + ((int64_t)b * Hq + h) * kD;
+    const float x1 = qr[threadIdx.x], x2 = qr[threadIdx.x + kD / 2];
+    qs[threadIdx.x] = (x1 * c - x2 * s) * 0.125f * kLog2e;
+    qs[threadIdx.x + kD / 2] = (x1 * s + x2 * c) * 0.125f * kLog2e;
+  }
+  __syncthreads();
+  float m = -INFINITY, l = 0.f, acc[kD];
+#pragma unroll
+  for (int d = 0; d < kD; ++d) acc[d] = 0.f;
+  for (int k = c0 + threadIdx.x; k < c1; k += 128) {
+    const int64_t row = ((int64_t)__ldg(indices + beg + k) * Hkv + g) * kD;
+    float sc = 0.f;
+#pragma unroll
+    for (int d = 0; d < kD; ++d) sc = fmaf(qs[d], __ldg(kp + row + d), sc);
+    const float mn = fmaxf(m, sc);
+    const float a = exp2f(m - mn), e = exp2f(sc - mn);
+    l = l * a + e;
+#pragma unroll
+    for (int d = 0; d < kD; ++d) acc[d] = fmaf(acc[d], a, e * __ldg(vp + row + d));
+    m = mn;
+  }
+  // block merge
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float M = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+  float L = l * f;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+#pragma unroll
+  for (int d = 0; d < kD; ++d) {
+    float x = acc[d] * f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) red_o[warp][d] = x;
+  }
+  if (lane == 0) {
+    red_m[warp] = M;
+    red_l[warp] = L;
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    float MM = -INFINITY;
+    for (int w = 0; w < 4; ++w) MM = fmaxf(MM, red_m[w]);
+    const float Mr = MM == -INFINITY ? 0.f : MM;
+    float LL = 0.f, x = 0.f;
+    for (int w = 0; w < 4; ++w) {
+      const float ff = exp2f(red_m[w] - Mr);
+      LL += red_l[w] * ff;
+      x += red_o[w][threadIdx.x] * ff;
+    }
+    const int64_t pi = ((int64_t)b * Hq + h) * ns + split;
+    part.o[pi * kD + threadIdx.x] = x;
+    if (threadIdx.x == 0) {
+      part.ml[2 * pi] = MM;
+      part.ml[2 * pi + 1] = LL;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kD) decode_combine_kernel(int Hq, int ns, const int32_t *indptr,
+                                                            Partials part, T *out) {
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int n = indptr[b + 1] - indptr[b];
+  const int used = n <= 0 ? 0 : min(ns, (n + kChunk - 1) / kChunk);
+  const int64_t base = ((int64_t)b * Hq + h) * ns;
+  float M = -INFINITY;
+  for (int s = 0; s < used; ++s) M = fmaxf(M, part.ml[2 * (base + s)]);
+  const float Mr = M == -INFINITY ? 0.f : M;
+  float L = 0.f, x = 0.f;
+  for (int s = 0; s < used; ++s) {
+    const float f = exp2f(part.ml[2 * (base + s)] - Mr);
+    L += part.ml[2 * (base + s) + 1] * f;
+    x += part.o[(base + s) * kD + d] * f;
+  }
+  const float y = L > 0.f ? x / L : 0.f;
+  T *o = out + ((int64_t)b * Hq + h) * kD + d;
+  if constexpr (sizeof(T) == 4) *o = y;
+  else *o = __float2bfloat16_rn(y);
+}
+
+}  // namespace
+
+size_t decode_partials_bytes(int B, int Hq, int max_kv) {
+  const int ns = n_splits(max_kv);
+  const size_t ml = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
+  const size_t o = ((size_t)B * Hq * ns * kD * 4 + 255) / 256 * 256;
+  return ml + o;
+}
+
+cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, const int32_t *qpos,
+                          const void *kp, const void *vp, const int32_t *indptr,
+                          const int32_t *indices, int max_kv, void *out, void *ws,
+                          const RopeTheta &th, cudaStream_t s) {
+  const int ns = n_splits(max_kv);
+  Partials part = partials(ws, B, Hq, max_kv);
+  if (dtype == AKV_BF16) {
+    constexpr int smem = kWarps * kStages * 4096;
+    static bool attr = false;  // once per process (single device use)
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    dim3 grid(ns, Hkv, B);
+    decode_bf16_kernel<<<grid, kWarps * 32, smem, s>>>(
+        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
+        (const __nv_bfloat16 *)vp, indptr, indices, part, th);
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part,
+                                                                    (__nv_bfloat16 *)out);
+  } else {
+    dim3 grid(ns, Hq, B);
+    decode_f32_kernel<<<grid, 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos, (const float *)kp,
+                                          (const float *)vp, indptr, indices, part, th);
+    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part, (float *)out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace akv

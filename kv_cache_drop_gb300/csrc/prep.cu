@@ -1,0 +1,112 @@
+// Restoration pre-pass (paper review page, Appendix A.1.1: "per-segment
+// temporary KV versions made by key rotation and value copy").
+//
+//  * Qr[h][t]     = R(pos(t)) Q[t][h]            rows in logical order
+//  * Kr[v][g][j]  = R(pos_v(src(j))) K[src(j)][g] one copy per key version,
+//                                                  slots in the plan's order
+//  * Vp[g][j]     = V[src(j)][g]                  values copied once, shared
+//                                                  by every version
+// For bf16 inputs the rotated copies Qr and Kr are written as fp16: the
+// rotation's output is not a bf16 value anyway, and fp16 keeps 3 more
+// mantissa bits for the score contraction at the same tensor-core rate.
+// An output beyond the fp16 range sets status bit kStatusFp16Range.
+// Outputs are head-major so that a 128-row tile of one head is 16 KiB of
+// contiguous memory (one TMA box).  Each CTA takes 32 rows, computes their
+// 32 x 32 cos/sin table once in shared memory, and streams 16-byte chunks.
+#include "common.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kRows = 32;
+constexpr int kThreads = 256;
+
+template <typename T, typename TR>
+__global__ void __launch_bounds__(kThreads) prep_q_kernel(PlanDev p, const T *__restrict__ q,
+                                                          RopeTheta th) {
+  constexpr int H = (kD / 2) / Chunk<T>::kElems;
+  bool ovf = false;
+  __shared__ float cs[kRows][kD / 2], sn[kRows][kD / 2];
+  const int64_t t0 = (int64_t)blockIdx.x * kRows;
+  for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
+    const int r = i / (kD / 2), f = i % (kD / 2);
+    if (t0 + r < p.T) rope_cs(th.th[f], (double)p.tok_qpos[t0 + r], &cs[r][f], &sn[r][f]);
+  }
+  __syncthreads();
+  const int units = kRows * p.Hq * H;
+  for (int u = threadIdx.x; u < units; u += kThreads) {
+    const int c = u % H, r = (u / H) % kRows, h = u / (H * kRows);
+    const int64_t t = t0 + r;
+    if (t >= p.T) continue;
+    const T *src = q + (t * p.Hq + h) * kD;
+    TR *dst = reinterpret_cast<TR *>(p.qr) + ((int64_t)h * p.T + t) * kD;
+    ovf |= rotate_pair<T, TR>(src, dst, c, cs[r], sn[r]);
+  }
+  if (sizeof(TR) == 2 && ovf) atomicOr(p.status, kStatusFp16Range);
+}
+
+template <typename T, typename TR>
+__global__ void __launch_bounds__(kThreads) prep_kv_kernel(PlanDev p, const T *__restrict__ k,
+                                                           const T *__restrict__ v,
+                                                           RopeTheta th) {
+  bool ovf = false;
+  constexpr int E = Chunk<T>::kElems;
+  constexpr int H = (kD / 2) / E;
+  __shared__ float cs[kRows][kD / 2], sn[kRows][kD / 2];
+  __shared__ int32_t src[kRows];
+  const int plane = blockIdx.y;  // < max_ver: key version; == max_ver: values
+  const int64_t j0 = (int64_t)blockIdx.x * kRows;
+  if (threadIdx.x < kRows && j0 + threadIdx.x < p.T) src[threadIdx.x] = p.slot_src[j0 + threadIdx.x];
+  if (plane < p.max_ver) {
+    for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
+      const int r = i / (kD / 2), f = i % (kD / 2);
+      if (j0 + r < p.T)
+        rope_cs(th.th[f], (double)p.slot_pos[(int64_t)plane * p.T + j0 + r], &cs[r][f],
+                &sn[r][f]);
+    }
+  }
+  __syncthreads();
+  if (plane < p.max_ver) {
+    TR *kr = reinterpret_cast<TR *>(p.kr) + (int64_t)plane * p.Hkv * p.T * kD;
+    const int units = kRows * p.Hkv * H;
+    for (int u = threadIdx.x; u < units; u += kThreads) {
+      const int c = u % H, r = (u / H) % kRows, g = u / (H * kRows);
+      const int64_t j = j0 + r;
+      if (j >= p.T) continue;
+      ovf |= rotate_pair<T, TR>(k + ((int64_t)src[r] * p.Hkv + g) * kD,
+                                kr + ((int64_t)g * p.T + j) * kD, c, cs[r], sn[r]);
+    }
+    if (sizeof(TR) == 2 && ovf) atomicOr(p.status, kStatusFp16Range);
+  } else {
+    constexpr int C = kD / E;  // chunks per row
+    const int units = kRows * p.Hkv * C;
+    for (int u = threadIdx.x; u < units; u += kThreads) {
+      const int c = u % C, r = (u / C) % kRows, g = u / (C * kRows);
+      const int64_t j = j0 + r;
+      if (j >= p.T) continue;
+      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + ((int64_t)src[r] * p.Hkv + g) * kD) + c);
+      reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.vp) + ((int64_t)g * p.T + j) * kD)[c] = x;
+    }
+  }
+}
+
+template <typename T, typename TR>
+cudaError_t prep(const PlanDev &p, const void *q, const void *k, const void *v,
+                 const RopeTheta &th, cudaStream_t s) {
+  const unsigned nb = (unsigned)((p.T + kRows - 1) / kRows);
+  prep_q_kernel<T, TR><<<nb, kThreads, 0, s>>>(p, (const T *)q, th);
+  dim3 g2(nb, p.max_ver + 1);
+  prep_kv_kernel<T, TR><<<g2, kThreads, 0, s>>>(p, (const T *)k, (const T *)v, th);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PlanDev &p, const void *q, const void *k, const void *v,
+                        const RopeTheta &th, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  return p.dtype == AKV_F32 ? prep<float, float>(p, q, k, v, th, s)
+                            : prep<__nv_bfloat16, __half>(p, q, k, v, th, s);
+}
+
+}  // namespace akv

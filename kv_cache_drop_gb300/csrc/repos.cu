@@ -1,0 +1,93 @@
+// Repos rotate + compact and append (paper review page section 3.3: a cached
+// key moves from position p to q by the rotation R(q - p), its value is left
+// as it is; section 4.2 / Appendix A.1.2: a key cached at another position
+// version is converted by key rotation).
+//
+// One streaming pass: every surviving row is read once (K and V, 16-byte
+// vector loads) and written once to its compacted place.  A CTA takes 32
+// rows; their 32 x 32 cos/sin table is built once in shared memory and shared
+// by all KV heads.
+#include "common.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kRows = 32;
+constexpr int kThreads = 256;
+
+template <typename T, bool kScatter>
+__global__ void __launch_bounds__(kThreads)
+    move_rows_kernel(int Hkv, int n, const int32_t *__restrict__ src, const int32_t *__restrict__ pf,
+                     const int32_t *__restrict__ pt, const T *__restrict__ kin,
+                     const T *__restrict__ vin, T *__restrict__ kout, T *__restrict__ vout,
+                     RopeTheta th) {
+  constexpr int E = Chunk<T>::kElems;
+  constexpr int H = (kD / 2) / E;  // chunk pairs per head row
+  constexpr int C = kD / E;        // chunks per head row
+  __shared__ float cs[kRows][kD / 2], sn[kRows][kD / 2];
+  __shared__ int64_t in_row[kRows], out_row[kRows];
+  const int j0 = blockIdx.x * kRows;
+  if (threadIdx.x < kRows) {
+    const int j = j0 + threadIdx.x;
+    if (j < n) {
+      // kScatter (append): row j of the inputs goes to pool slot src[j],
+      // rotated to absolute position pf[j].  Otherwise (repos): pool row
+      // src[j] goes to compact row j, rotated by pos_to - pos_from.
+      in_row[threadIdx.x] = kScatter ? j : src[j];
+      out_row[threadIdx.x] = kScatter ? src[j] : j;
+    }
+  }
+  for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
+    const int r = i / (kD / 2), f = i % (kD / 2);
+    const int j = j0 + r;
+    if (j < n) {
+      const double delta = kScatter ? (double)pf[j] : (double)((pt ? pt[j] : j) - pf[j]);
+      rope_cs(th.th[f], delta, &cs[r][f], &sn[r][f]);
+    }
+  }
+  __syncthreads();
+  const int rows = min(kRows, n - j0);
+  const int k_units = rows * Hkv * H;
+  for (int u = threadIdx.x; u < k_units; u += kThreads) {
+    const int c = u % H, r = (u / H) % rows, g = u / (H * rows);
+    rotate_pair<T>(kin + (in_row[r] * Hkv + g) * kD, kout + (out_row[r] * Hkv + g) * kD, c, cs[r],
+                   sn[r]);
+  }
+  const int v_units = rows * Hkv * C;
+  for (int u = threadIdx.x; u < v_units; u += kThreads) {
+    const int c = u % C, row = u / C;  // row = r * Hkv + g, consecutive in memory
+    const int r = row / Hkv, g = row % Hkv;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(vin + (in_row[r] * Hkv + g) * kD) + c);
+    reinterpret_cast<uint4 *>(vout + (out_row[r] * Hkv + g) * kD)[c] = x;
+  }
+}
+
+template <typename T, bool kScatter>
+cudaError_t move_rows(int Hkv, int n, const int32_t *src, const int32_t *pf, const int32_t *pt,
+                      const void *kin, const void *vin, void *kout, void *vout,
+                      const RopeTheta &th, cudaStream_t s) {
+  const unsigned nb = (unsigned)((n + kRows - 1) / kRows);
+  move_rows_kernel<T, kScatter><<<nb, kThreads, 0, s>>>(Hkv, n, src, pf, pt, (const T *)kin,
+                                                       (const T *)vin, (T *)kout, (T *)vout, th);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_repos(int dtype, int Hkv, int r, const int32_t *src, const int32_t *pf,
+                         const int32_t *pt, const void *kin, const void *vin, void *kout,
+                         void *vout, const RopeTheta &th, cudaStream_t s) {
+  return dtype == AKV_F32
+             ? move_rows<float, false>(Hkv, r, src, pf, pt, kin, vin, kout, vout, th, s)
+             : move_rows<__nv_bfloat16, false>(Hkv, r, src, pf, pt, kin, vin, kout, vout, th, s);
+}
+
+cudaError_t launch_append(int dtype, int Hkv, int n, const void *kn, const void *vn,
+                          const int32_t *pos, const int32_t *slot, void *kp, void *vp,
+                          const RopeTheta &th, cudaStream_t s) {
+  return dtype == AKV_F32
+             ? move_rows<float, true>(Hkv, n, slot, pos, nullptr, kn, vn, kp, vp, th, s)
+             : move_rows<__nv_bfloat16, true>(Hkv, n, slot, pos, nullptr, kn, vn, kp, vp, th, s);
+}
+
+}  // namespace akv

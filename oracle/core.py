@@ -37,7 +37,9 @@ class OpLogError(ValueError):
 
 
 def widen(x: np.ndarray, dtype: str) -> np.ndarray:
-    """float32 values or bfloat16 bit patterns -> float64 (exact)."""
+    """float32 values or bfloat16 bit patterns -> float64 (exact); "f64" passes through."""
+    if dtype == "f64":
+        return np.asarray(x, dtype=np.float64)
     if dtype == "f32":
         return np.asarray(x, dtype=np.float32).astype(np.float64)
     if dtype == "bf16":

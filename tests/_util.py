@@ -1,0 +1,80 @@
+"""Helpers shared by the GPU parity tests: move seeded inputs to the device,
+run the C-ABI calls, and compare with the oracle."""
+import numpy as np
+
+import kv_cache_drop_gb300 as akv
+import oracle
+
+BF16_MAX_ABS = 2e-2        # bf16 inputs, fp32 accumulation
+BF16_REL_RMS = 2.0 ** -7   # error RMS / reference RMS
+F32_MAX_ABS = 1e-4
+
+
+def run_prefill(reqs, device="cuda"):
+    """Segment-batch prefill of a batch of requests; returns (out [T,Hq,D]
+    float32 numpy, plan, workspace)."""
+    import torch
+    r0 = reqs[0]
+    shp = akv.shape(r0.Hq, r0.Hkv, 64, r0.dtype, r0.rope_base)
+    cu = np.concatenate([[0], np.cumsum([r.T_prefill for r in reqs])]).astype(np.int32)
+    ops = []
+    for r in reqs:
+        n = r.n_msgs if r.n_prefill_msgs < 0 else r.n_prefill_msgs
+        keep_d = r.drop_after < n
+        ops.append((r.msg_start[:n + 1], r.drop_after[keep_d], r.drop_target[keep_d],
+                    r.repos_after[r.repos_after < n]))
+    plan = akv.Plan(shp, cu, ops)
+    q = akv.to_device(np.concatenate([r.q[:r.T_prefill] for r in reqs]), r0.dtype, device)
+    k = akv.to_device(np.concatenate([r.k[:r.T_prefill] for r in reqs]), r0.dtype, device)
+    v = akv.to_device(np.concatenate([r.v[:r.T_prefill] for r in reqs]), r0.dtype, device)
+    out = torch.zeros_like(q)
+    ws = plan.workspace(device)
+    akv.akv_segment_attention_run(plan, q, k, v, out, ws)
+    torch.cuda.synchronize()
+    assert akv.akv_workspace_status(ws) == 0, "a kernel barrier wait timed out"
+    return out.float().cpu().numpy(), plan, ws
+
+
+def oracle_rows(r, rows=None):
+    n = r.n_msgs if r.n_prefill_msgs < 0 else r.n_prefill_msgs
+    keep_d = r.drop_after < n
+    ops = (r.msg_start[:n + 1], r.drop_after[keep_d], r.drop_target[keep_d],
+           r.repos_after[r.repos_after < n])
+    T = r.T_prefill
+    out, _ = oracle.replay_attention(*ops, r.q[:T], r.k[:T], r.v[:T], r.dtype, r.rope_base,
+                                     rows=rows)
+    return out
+
+
+def err(got, ref):
+    d = np.abs(got.astype(np.float64) - ref)
+    rms_ref = float(np.sqrt(np.mean(ref * ref))) or 1.0
+    return float(d.max()), float(np.sqrt(np.mean(d * d)) / rms_ref)
+
+
+def assert_close(got, ref, dtype):
+    mx, rel = err(got, ref)
+    print(f"[parity] {dtype} max_abs={mx:.3e} rel_rms={rel:.3e}")
+    if dtype == "bf16":
+        assert mx <= BF16_MAX_ABS and rel <= BF16_REL_RMS, (mx, rel)
+    else:
+        assert mx <= F32_MAX_ABS, (mx, rel)
+    return mx, rel
+
+
+def sample_rows(r, n_random=24, seed=0):
+    """Rows at message and tile edges plus random ones."""
+    T = r.T_prefill
+    rng = np.random.default_rng(seed)
+    edges = {0, 1, T - 1, T - 2}
+    for m in range(1, len(r.msg_start) - 1):
+        s = int(r.msg_start[m])
+        if 0 < s < T:
+            edges.update({s - 1, s})
+    edges = sorted(e for e in edges if 0 <= e < T)
+    pick = list(rng.choice(edges, size=min(len(edges), n_random), replace=False))
+    pick += list(rng.integers(0, T, size=n_random))
+    for t0 in (127, 128, 129):
+        if t0 < T:
+            pick.append(t0)
+    return np.unique(np.array(pick, dtype=np.int64))

@@ -1,0 +1,229 @@
+"""Compaction, repos rotation, append and decode on the GPU against the oracle,
+and the tiny fp32 workload end to end (prefill -> compact -> repos -> decode)."""
+import numpy as np
+import pytest
+
+import kv_cache_drop_gb300 as akv
+import oracle
+import workloads
+from _util import assert_close, oracle_rows, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _compact(ops, T, upto):
+    torch = _torch()
+    idx = torch.full((max(T, 1),), -1, dtype=torch.int32, device="cuda")
+    pos = torch.full((max(T, 1),), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(1, akv.akv_compact_workspace(ops, T)), dtype=torch.uint8, device="cuda")
+    n = akv.akv_compact(ops, T, upto, idx, pos, ws)
+    torch.cuda.synchronize()
+    return idx[:n].cpu().numpy(), pos[:n].cpu().numpy()
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_compact_every_boundary_bit_exact(seed):
+    r = workloads.random_request(70 + seed, n_msgs=10, max_len=3000 if seed < 2 else 40,
+                                 p_drop=0.3, p_repos=0.3)
+    for upto in list(range(r.n_msgs)) + [-1]:
+        gi, gp = _compact(r.ops(), r.T, upto)
+        ou, op = oracle.compact(*r.ops(), upto=upto)
+        np.testing.assert_array_equal(gi, ou)
+        np.testing.assert_array_equal(gp, op)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_repos_rotate(dtype):
+    torch = _torch()
+    rng = np.random.default_rng(5)
+    S, r, Hkv = 5000, 3000, 8
+    k = workloads.gen._normals(rng, (S, Hkv, 64), dtype)
+    v = workloads.gen._normals(rng, (S, Hkv, 64), dtype)
+    src = np.sort(rng.choice(S, size=r, replace=False)).astype(np.int32)
+    pf = rng.integers(0, 131072, size=r).astype(np.int32)
+    pt = np.arange(r, dtype=np.int32)
+    shp = akv.shape(16, Hkv, 64, dtype)
+    ko = torch.zeros((r, Hkv, 64), dtype=torch.bfloat16 if dtype == "bf16" else torch.float32,
+                     device="cuda")
+    vo = torch.zeros_like(ko)
+    for pos_to in (akv.i32_device(pt), None):
+        akv.akv_repos_rotate(shp, r, akv.i32_device(src), akv.i32_device(pf), pos_to,
+                             akv.to_device(k, dtype), akv.to_device(v, dtype), ko, vo)
+        torch.cuda.synchronize()
+        rk, rv = oracle.repos_rotate(k, v, src, pf, pt, dtype, 10000.0)
+        tol = 2 ** -8 * 4 if dtype == "bf16" else 1e-5
+        assert np.max(np.abs(ko.float().cpu().numpy() - rk)) <= tol
+        assert np.array_equal(vo.float().cpu().numpy(), rv)  # values copied bit for bit
+
+
+def test_repos_compact_full_size():
+    """128k trajectory: compact the survivors at the repos boundary and rotate
+    every one of them to its new position 0..r-1."""
+    torch = _torch()
+    r = workloads.repos_config()
+    b = int(r.repos_after[0])
+    idx, pos = _compact(r.ops(), r.T, b)
+    ou, op = oracle.compact(*r.ops(), upto=b)
+    np.testing.assert_array_equal(idx, ou)
+    np.testing.assert_array_equal(pos, op)
+    n = len(idx)
+    shp = akv.shape(64, 8, 64, "bf16")
+    ko = torch.empty((n, 8, 64), dtype=torch.bfloat16, device="cuda")
+    vo = torch.empty_like(ko)
+    akv.akv_repos_rotate(shp, n, akv.i32_device(idx), akv.i32_device(pos), None,
+                         akv.to_device(r.k, "bf16"), akv.to_device(r.v, "bf16"), ko, vo)
+    torch.cuda.synchronize()
+    rk, rv = oracle.repos_rotate(r.k, r.v, ou, op, np.arange(n), "bf16", 10000.0)
+    assert np.max(np.abs(ko.float().cpu().numpy() - rk)) <= 2 ** -8 * 4
+    assert np.array_equal(vo.float().cpu().numpy(), rv)
+
+
+def _decode_oracle(dw, step, q_step):
+    """Oracle decode at `step`: active pool keys as stored, appended keys
+    rotated by the oracle itself at their positions."""
+    out = []
+    for b in range(dw.B):
+        ka = oracle.widen(dw.k_pool[dw.active_slots[b]], dw.dtype)
+        va = oracle.widen(dw.v_pool[dw.active_slots[b]], dw.dtype)
+        pos = dw.L[b] + np.arange(step + 1)
+        kn = oracle.rope(oracle.widen(dw.k_new[:step + 1, b], dw.dtype), pos[:, None],
+                         dw.rope_base)
+        vn = oracle.widen(dw.v_new[:step + 1, b], dw.dtype)
+        K = np.concatenate([ka, kn])
+        V = np.concatenate([va, vn])
+        o = oracle.decode_attention(q_step[b:b + 1], np.array([dw.L[b] + step]), K, V,
+                                    np.array([0, len(K)]), np.arange(len(K)), "f64", dw.rope_base)
+        out.append(o[0])
+    return np.stack(out)
+
+
+def _run_decode(dw, check_steps):
+    torch = _torch()
+    shp = akv.shape(dw.Hq, dw.Hkv, 64, dw.dtype)
+    kp = akv.to_device(dw.k_pool, dw.dtype)
+    vp = akv.to_device(dw.v_pool, dw.dtype)
+    max_kv = max(len(a) for a in dw.active_slots) + dw.steps
+    ws = torch.empty(max(1, akv.akv_decode_workspace(shp, dw.B, max_kv)), dtype=torch.uint8,
+                     device="cuda")
+    results = {}
+    for step in range(dw.steps):
+        pos = akv.i32_device(dw.L + step)
+        akv.akv_append_kv(shp, dw.B, akv.to_device(dw.k_new[step], dw.dtype),
+                          akv.to_device(dw.v_new[step], dw.dtype), pos,
+                          akv.i32_device(dw.append_slots[step]), kp, vp)
+        indptr, idx = dw.indices_at(step)
+        q = akv.to_device(dw.q[step], dw.dtype)
+        out = torch.empty_like(q)
+        akv.akv_decode_attention(shp, dw.B, q, pos, kp, vp, akv.i32_device(indptr),
+                                 akv.i32_device(idx), max_kv, out, ws)
+        if step in check_steps:
+            torch.cuda.synchronize()
+            results[step] = out.float().cpu().numpy()
+    return results
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_small(dtype):
+    dw = workloads.decode_workload(seed=8, B=3, active=(100, 5000), steps=3, Hq=8, Hkv=2,
+                                   dtype=dtype)
+    res = _run_decode(dw, {0, 1, 2})
+    for step, got in res.items():
+        qf = oracle.widen(dw.q[step], dtype)
+        assert_close(got, _decode_oracle(dw, step, qf), dtype)
+
+
+def test_decode_peaky_and_empty_request():
+    torch = _torch()
+    dw = workloads.decode_workload(seed=9, B=2, active=(3000, 6000), steps=1, Hq=16, Hkv=2)
+    dw.q[0] = workloads.bf16_bits(oracle.widen(dw.q[0], "bf16").astype(np.float32) * 8)
+    res = _run_decode(dw, {0})
+    assert_close(res[0], _decode_oracle(dw, 0, oracle.widen(dw.q[0], "bf16")), "bf16")
+    # a request with no keys gets zeros
+    shp = akv.shape(16, 2, 64, "bf16")
+    q = akv.to_device(dw.q[0], "bf16")
+    out = torch.full_like(q, 7.0)
+    ws = torch.empty(akv.akv_decode_workspace(shp, 2, 10), dtype=torch.uint8, device="cuda")
+    akv.akv_decode_attention(shp, 2, q, akv.i32_device([5, 5]), akv.to_device(dw.k_pool, "bf16"),
+                             akv.to_device(dw.v_pool, "bf16"), akv.i32_device([0, 0, 0]),
+                             akv.i32_device([0]), 10, out, ws)
+    torch.cuda.synchronize()
+    assert float(out.abs().max()) == 0.0
+
+
+def test_decode_full_size_steps():
+    """14 requests, 20k-90k active keys each, 256 decode steps with appends;
+    steps 0, 1 and 255 checked in full."""
+    dw = workloads.decode_workload()
+    res = _run_decode(dw, {0, 1, dw.steps - 1})
+    for step, got in res.items():
+        assert_close(got, _decode_oracle(dw, step, oracle.widen(dw.q[step], "bf16")), "bf16")
+
+
+def test_tiny_fp32_end_to_end():
+    """User 16 / assistant 24 / tool 32 with drop {1:[0], 2:[1]}, reposition
+    [2], then 8 decode appends: attention outputs, the active-index list and
+    the post-repos keys."""
+    torch = _torch()
+    r = workloads.tiny_config()
+    shp = akv.shape(2, 2, 64, "f32")
+    Tp = r.T_prefill
+    got, plan, _ = run_prefill([r])
+    ref_all, _ = oracle.replay_attention(*r.ops(), r.q, r.k, r.v, "f32", r.rope_base)
+    assert_close(got, ref_all[:Tp], "f32")
+    # keys of the prefill go to a pool at their append positions
+    kp = torch.zeros((256, 2, 64), dtype=torch.float32, device="cuda")
+    vp = torch.zeros_like(kp)
+    tpos = plan.tables()["tok_pos"]
+    akv.akv_append_kv(shp, Tp, akv.to_device(r.k[:Tp], "f32"), akv.to_device(r.v[:Tp], "f32"),
+                      akv.i32_device(tpos), akv.i32_device(np.arange(Tp)), kp, vp)
+    # compact at the boundary after message 2 and re-position the survivors
+    ops3 = (r.msg_start[:4], r.drop_after, r.drop_target, r.repos_after)
+    idx, pos = _compact(ops3, Tp, 2)
+    np.testing.assert_array_equal(idx, np.arange(40, 72))
+    np.testing.assert_array_equal(pos, np.arange(40, 72))
+    n = len(idx)
+    base = 100  # the compacted cache lives at pool slots 100..
+    akv.akv_repos_rotate(shp, n, akv.i32_device(idx), akv.i32_device(pos), None, kp, vp,
+                         kp[base:base + n], vp[base:base + n])
+    torch.cuda.synchronize()
+    ref_k = oracle.rope(oracle.widen(r.k[idx], "f32"), np.arange(n)[:, None], r.rope_base)
+    assert np.max(np.abs(kp[base:base + n].cpu().numpy() - ref_k)) <= 1e-4
+    # eight decode steps over the compacted cache
+    ws = torch.empty(akv.akv_decode_workspace(shp, 1, 64), dtype=torch.uint8, device="cuda")
+    for i in range(8):
+        t = Tp + i
+        p = n + i
+        akv.akv_append_kv(shp, 1, akv.to_device(r.k[t:t + 1], "f32"),
+                          akv.to_device(r.v[t:t + 1], "f32"), akv.i32_device([p]),
+                          akv.i32_device([base + p]), kp, vp)
+        out = torch.empty((1, 2, 64), dtype=torch.float32, device="cuda")
+        akv.akv_decode_attention(shp, 1, akv.to_device(r.q[t:t + 1], "f32"), akv.i32_device([p]),
+                                 kp, vp, akv.i32_device([0, p + 1]),
+                                 akv.i32_device(base + np.arange(p + 1)), 64, out, ws)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), ref_all[t:t + 1], "f32")
+    res = oracle.replay(*r.ops())
+    np.testing.assert_array_equal(res.active_u, np.arange(40, 80))
+
+
+def test_errors_are_reported_before_launch():
+    torch = _torch()
+    r = workloads.random_request(3, n_msgs=3, max_len=50, Hq=8, Hkv=2)
+    plan = akv.Plan(akv.shape(8, 2, 64, "bf16"), [0, r.T], [r.ops()])
+    q = akv.to_device(r.q, "bf16")
+    k = akv.to_device(r.k, "bf16")
+    v = akv.to_device(r.v, "bf16")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(akv.AkvError) as e:
+        akv.akv_segment_attention_run(plan, q, k, v, torch.empty_like(q), small)
+    assert e.value.status == 3
+    with pytest.raises(akv.AkvError) as e:
+        akv.Plan(akv.shape(6, 2, 64, "bf16"), [0, r.T], [r.ops()]).__class__  # valid plan
+        p2 = akv.Plan(akv.shape(6, 2, 64, "bf16"), [0, r.T], [r.ops()])
+        akv.akv_segment_attention_run(p2, q, k, v, torch.empty_like(q), p2.workspace())
+    assert e.value.status == 4  # odd query heads per KV head in bf16

@@ -1,0 +1,98 @@
+"""Segment-batch restoration prefill on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import workloads
+from _util import assert_close, oracle_rows, run_prefill, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefill_bf16_random_logs(seed):
+    r = workloads.random_request(10 + seed, n_msgs=8, max_len=260, Hq=8, Hkv=2, dtype="bf16",
+                                 p_drop=0.3, p_repos=0.25)
+    got, _, _ = run_prefill([r])
+    assert_close(got, oracle_rows(r), "bf16")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_prefill_bf16_peaky_scores(seed):
+    """Queries scaled by 8: score std ~8, so the softmax is far from flat."""
+    r = workloads.random_request(20 + seed, n_msgs=7, max_len=300, Hq=8, Hkv=2, dtype="bf16",
+                                 p_drop=0.3, p_repos=0.3, q_scale=8.0)
+    got, _, _ = run_prefill([r])
+    assert_close(got, oracle_rows(r), "bf16")
+
+
+def test_prefill_bf16_gqa_64_8_ragged_batch():
+    reqs = [workloads.random_request(30 + i, n_msgs=4 + i, max_len=200, Hq=64, Hkv=8,
+                                     dtype="bf16", p_drop=0.3, p_repos=0.3, min_len=1)
+            for i in range(3)]
+    got, plan, _ = run_prefill(reqs)
+    off = 0
+    for r in reqs:
+        assert_close(got[off:off + r.T], oracle_rows(r), "bf16")
+        off += r.T
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 256, 300])
+def test_prefill_tile_edges(T):
+    ms = np.array([0, T // 3, T // 3, T], dtype=np.int32)  # includes an empty message
+    r = workloads.random_request(40, n_msgs=3, max_len=1, Hq=4, Hkv=2, dtype="bf16")
+    rr = workloads.gen._trajectory("edge", 41, ms, ["m"] * 3, [(1, 0)], [1], 4, 2, 64, "bf16")
+    got, _, _ = run_prefill([rr])
+    assert_close(got, oracle_rows(rr), "bf16")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefill_f32_random_logs(seed):
+    r = workloads.random_request(50 + seed, n_msgs=7, max_len=60, Hq=4, Hkv=2, dtype="f32",
+                                 p_drop=0.3, p_repos=0.3)
+    got, _, _ = run_prefill([r])
+    assert_close(got, oracle_rows(r), "f32")
+
+
+def test_visible_counts_bit_exact():
+    import torch
+    import kv_cache_drop_gb300 as akv
+    import oracle
+    reqs = [workloads.random_request(60 + i, n_msgs=9, max_len=400, Hq=8, Hkv=2, dtype="bf16",
+                                     p_drop=0.35, p_repos=0.25) for i in range(4)]
+    _, plan, ws = run_prefill(reqs)
+    counts = torch.zeros(plan.info["T"], dtype=torch.int32, device="cuda")
+    akv.akv_segment_visible_counts(plan, counts, ws)
+    got = counts.cpu().numpy()
+    ref = np.concatenate([oracle.visible_counts(*r.ops()) for r in reqs])
+    np.testing.assert_array_equal(got, ref)
+    assert int(got.sum()) == plan.info["visible_pairs"]
+
+
+def test_prefill_rolling_drop_medium():
+    """25 rounds of the agent trajectory at the GQA 64/8 shape, sampled rows."""
+    r = workloads.rolling_drop_config(rounds=25)
+    got, _, _ = run_prefill([r])
+    rows = sample_rows(r, 16)
+    assert_close(got[rows], oracle_rows(r, rows), "bf16")
+
+
+def test_prefill_rolling_drop_full_size():
+    """The full 100-round trajectory (bench configuration), sampled rows."""
+    r = workloads.rolling_drop_config()
+    got, plan, _ = run_prefill([r])
+    rows = sample_rows(r, 12, seed=1)
+    assert_close(got[rows], oracle_rows(r, rows), "bf16")
+    assert np.isfinite(got).all()
+
+
+def test_prefill_repos_full_size():
+    """128k tokens with a repos at 96k: both key versions, sampled rows."""
+    r = workloads.repos_config()
+    assert len(r.repos_after) >= 1
+    got, plan, _ = run_prefill([r])
+    assert plan.info["max_versions"] == 1 + len(r.repos_after)
+    rows = sample_rows(r, 12, seed=2)
+    b = int(r.msg_start[r.repos_after[0] + 1])  # first row of version 1
+    rows = np.unique(np.concatenate([rows, [b - 1, b, b + 1, b + 200]]))
+    assert_close(got[rows], oracle_rows(r, rows), "bf16")
+    assert np.isfinite(got).all()
