@@ -214,6 +214,36 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
                                 int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
                                 akv_stream_t stream);
 
+/* Decode without a workspace.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory, so cannot
+ * pass the workspace akv_decode_attention needs -- for example a plug-in
+ * running inside a host framework that owns the whole device memory pool and
+ * gives plug-ins no allocation hook, or a request path that must not
+ * allocate per call.  Same arguments, semantics and results as
+ * akv_decode_attention, minus the workspace: the split-KV partials go to a
+ * fixed array in the library's device memory,
+ * akv_decode_static_scratch_bytes() bytes (16 MiB) on every GPU that loads
+ * the library, held until the process exits.  Nothing is allocated by the
+ * call (no cudaMalloc/cudaFree, no allocating library routine).
+ *  - Limit: decode_partials(B, Hq, max_kv) = B * Hq * ceil(max_kv / 2048) *
+ *    66 * 4 bytes (each part rounded up to 256) must fit the array; larger
+ *    requests return AKV_ERR_UNSUPPORTED with the sizes in akv_last_error(),
+ *    before anything is enqueued.
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address with cudaGetSymbolAddress and caches it; make
+ *    that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array.  Calls that
+ *    overlap on the GPU (other streams, other host threads) race and corrupt
+ *    each other's results; serialise them.  The array keeps the last call's
+ *    contents; nothing in it needs to start at zero (each call writes every
+ *    partial it later reads). */
+akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
+                                       const int32_t *q_pos, const void *k_pool,
+                                       const void *v_pool, const int32_t *kv_indptr,
+                                       const int32_t *kv_indices, int32_t max_kv, void *out,
+                                       akv_stream_t stream);
+size_t akv_decode_static_scratch_bytes(void);
+
 /* Append (section 3.3): for i in 0..n-1, k_pool[slot[i]] = R(pos[i]) *
  * k_new[i] and v_pool[slot[i]] = v_new[i].  k_new/v_new: device [n, Hkv, D]
  * raw; pos, slot: device int32 [n]; slots must be distinct. */

@@ -95,6 +95,10 @@ _SIGS = {
                              [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_void_p,
                                                       ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "akv_decode_attention_static": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
+                                    [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_void_p,
+                                                             ctypes.c_void_p]),
+    "akv_decode_static_scratch_bytes": (ctypes.c_size_t, []),
     "akv_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
                       [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),
 }
@@ -293,6 +297,20 @@ def akv_decode_attention(shp: Shape, B: int, q, q_pos, k_pool, v_pool, kv_indptr
                                       _dev(out), _dev(workspace),
                                       0 if workspace is None else workspace.numel(),
                                       _stream(stream)))
+
+
+def akv_decode_attention_static(shp: Shape, B: int, q, q_pos, k_pool, v_pool, kv_indptr,
+                                kv_indices, max_kv: int, out, stream=None):
+    """Decode with the split-KV partials in the library's static device array
+    (no workspace; see include/akv.h for the size limit and sharing rules)."""
+    _check(lib().akv_decode_attention_static(ctypes.byref(shp), B, _dev(q), _dev(q_pos),
+                                             _dev(k_pool), _dev(v_pool), _dev(kv_indptr),
+                                             _dev(kv_indices), max_kv, _dev(out),
+                                             _stream(stream)))
+
+
+def akv_decode_static_scratch_bytes() -> int:
+    return lib().akv_decode_static_scratch_bytes()
 
 
 def akv_append_kv(shp: Shape, n: int, k_new, v_new, pos, slot, k_pool, v_pool, stream=None):

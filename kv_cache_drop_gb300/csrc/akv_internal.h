@@ -96,4 +96,12 @@ cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, cons
                           const int32_t *indices, int max_kv, void *out, void *ws,
                           const RopeTheta &th, cudaStream_t s);
 
+// Decode with its split-KV partials in a static device array (no workspace).
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+cudaError_t decode_static_scratch(void **ptr);
+cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *q,
+                                 const int32_t *qpos, const void *kp, const void *vp,
+                                 const int32_t *indptr, const int32_t *indices, int max_kv,
+                                 void *out, const RopeTheta &th, cudaStream_t s);
+
 }  // namespace akv

@@ -736,4 +736,35 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
   return AKV_OK;
 }
 
+akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
+                                       const int32_t *q_pos, const void *k_pool,
+                                       const void *v_pool, const int32_t *kv_indptr,
+                                       const int32_t *kv_indices, int32_t max_kv, void *out,
+                                       akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_decode_attention_static")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B == 0) return AKV_OK;
+  if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out || (max_kv > 0 && !kv_indices))
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
+  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv);
+  if (need > kStaticScratchBytes)
+    return fail(AKV_ERR_UNSUPPORTED,
+                "akv_decode_attention_static: B=%d, Hq=%d, max_kv=%d need %zu bytes of split-KV "
+                "partials but the static scratch holds %zu; use akv_decode_attention with a "
+                "workspace",
+                B, shape->Hq, max_kv, need, kStaticScratchBytes);
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_decode_static(shape->dtype, B, shape->Hq, shape->Hkv, q, q_pos, k_pool,
+                                       v_pool, kv_indptr, kv_indices, max_kv, out, th,
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode (static scratch)");
+  return AKV_OK;
+}
+
+size_t akv_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
 }  // extern "C"

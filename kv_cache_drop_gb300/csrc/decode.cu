@@ -17,6 +17,8 @@
 // fp32: one thread per key, FMA dot products, block-level merge.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace akv {
 namespace {
 
@@ -437,6 +439,64 @@ cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, cons
     dim3 grid(ns, Hq, B);
     decode_f32_kernel<<<grid, 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos, (const float *)kp,
                                           (const float *)vp, indptr, indices, part, th);
+    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part, (float *)out);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller workspace.  The split-KV partials go to a fixed
+// array in this module's device memory instead: every GPU that loads the
+// library keeps kStaticScratchBytes for it until the process exits.  Host
+// code cannot pass the array's name to a kernel (on the host it is only a
+// stand-in, not a device address), so its address is looked up once per
+// device with cudaGetSymbolAddress and cached.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+}  // namespace
+
+cudaError_t decode_static_scratch(void **ptr) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *q,
+                                 const int32_t *qpos, const void *kp, const void *vp,
+                                 const int32_t *indptr, const int32_t *indices, int max_kv,
+                                 void *out, const RopeTheta &th, cudaStream_t s) {
+  void *scratch = nullptr;
+  cudaError_t e = decode_static_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  const int ns = n_splits(max_kv);
+  Partials part = partials(scratch, B, Hq, max_kv);
+  if (dtype == AKV_BF16) {
+    constexpr int smem = kWarps * kStages * 4096;
+    e = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
+        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
+        (const __nv_bfloat16 *)vp, indptr, indices, part, th);
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part,
+                                                                    (__nv_bfloat16 *)out);
+  } else {
+    decode_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos,
+                                                      (const float *)kp, (const float *)vp,
+                                                      indptr, indices, part, th);
     decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part, (float *)out);
   }
   return cudaGetLastError();
