@@ -168,8 +168,8 @@ akv_status akv_segment_visible_counts(const akv_plan *plan, int32_t *counts, voi
  * calls above (synchronises `stream`).  *code = 0 when no kernel reported a
  * failure; otherwise a bit mask and the call returns AKV_ERR_DEVICE:
  *   1  a barrier wait in a kernel gave up (its outputs are not valid);
- *   2  (bf16) a rotated query or key exceeded the fp16 range of the score
- *      operands (|value| > 65504) and was saturated. */
+ *   2  (bf16) a rotated query or key, or a value, exceeded the fp16 range
+ *      of the tensor-core operands (|value| > 65504). */
 akv_status akv_workspace_status(void *workspace, akv_stream_t stream, uint32_t *code);
 
 /* ------------------------------------------------------------------------

@@ -47,6 +47,7 @@ struct PlanDev {
   void *kr;                  // [max_ver][Hkv][T][D] rotated keys, permuted slots, head-major
                              // (fp16 for bf16 inputs)
   void *vp;                  // [Hkv][T][D] values, permuted slots, head-major
+                             // (fp16 for bf16 inputs)
   int64_t T;
   int32_t n_qtiles;
   int32_t max_ver;

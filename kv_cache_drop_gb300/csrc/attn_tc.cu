@@ -1,8 +1,12 @@
 // bf16 segment-batch attention on the 5th-generation tensor cores (tcgen05,
 // TMEM accumulators, TMA loads), sm_103a.
 //
-// Operands: rotated Q and K are fp16 copies (see the pre-pass), P and V are
-// bf16; both products accumulate in fp32.
+// Operands: rotated Q and K and the permuted V are fp16 copies (see the
+// pre-pass); P is produced as fp16 by a packed fp16 exp; both products
+// accumulate in fp32.  Row sums of P come from the tensor core too: the PV
+// product runs with N = 80, its B operand being the V tile (columns 0-63)
+// followed by a constant tile of ones (columns 64-79), so column 64 of the
+// accumulator is the row sum and the softmax threads never add.
 //
 // What it computes (paper review page section 4.2, Appendix A.1.1): for each
 // query row t of a tile and each key slot j of the tile's 128-key windows,
@@ -16,11 +20,16 @@
 //   warp 8     TMA producer: Q tiles once, then K and V windows through a
 //              kStages-deep ring
 //   warp 9     TMEM allocator + single-thread tcgen05.mma issuer
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384).
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,336) O1 [336,416)
+// (O columns 64-79 hold the row sum).  P_i (fp16, two per 32-bit column)
+// overwrites the first 64 columns of S_i once S_i is in registers, and the
+// PV product reads it from there (A operand in TMEM): P never touches shared
+// memory, whose bandwidth the K=16 MMAs would otherwise saturate.  S_i(n+1)
+// is issued after PV_i(n) by the same thread, and tcgen05.mma operations of
+// one thread execute in issue order, so it cannot overwrite P_i(n) early.
 // Per window n the issue order is S0(n) S1(n) | PV0(n) S0(n+1) PV1(n) S1(n+1):
 // while one softmax group turns S into P the tensor core works for the other.
-// P goes to shared memory as bf16 (128-byte swizzled, K-major); O stays in
-// TMEM for the whole tile.  The running max is only raised (and O rescaled)
+// O stays in TMEM for the whole tile.  The running max is only raised (and O rescaled)
 // when it grows by more than 2^8, so O is rarely touched.
 // Every barrier wait is bounded; a timeout sets a bit in the workspace status
 // word, after which all waits in the grid return at once so the launch ends.
@@ -32,7 +41,7 @@
 namespace akv {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 3;  // the V-descriptor selection below assumes 3
 constexpr int kThreads = 320;
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTileBytes = 128 * 64 * 2;  // 128 rows x 64 bf16
@@ -45,7 +54,7 @@ struct __align__(1024) Smem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint8_t p[2][2][kTileBytes];  // [head][key half]
+  uint8_t ones[kTileBytes];     // fp16 1.0, right after v: second MN atom of the PV B operand
   int32_t mask_u[2][2][128];    // [head][buffer][column]
   int32_t mask_d[2][2][128];
   uint64_t bar_q;
@@ -66,12 +75,6 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_
 __device__ __forceinline__ uint64_t desc_k_major(uint32_t saddr) {
   return ptx::sdesc_sw128(saddr);
 }
-// MN-major operand (V: keys along K, head dim along N): 8-key groups 1024 B
-// apart; the same value is written to both stride fields.
-__device__ __forceinline__ uint64_t desc_mn_major(uint32_t saddr) {
-  return ptx::sdesc_sw128(saddr, 1024);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -107,6 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&sm.bar_done, 1);
     ptx::fence_barrier_init();
   }
+  {
+    uint4 *o = reinterpret_cast<uint4 *>(sm.ones);
+    const uint4 one8 = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    for (int i = threadIdx.x; i < (int)(kTileBytes / 16); i += kThreads) o[i] = one8;
+    ptx::fence_proxy_async_smem();  // visible to the tensor core
+  }
   if (warp == kMmaWarp) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
   if (warp == kProdWarp && lane == 0) {
     ptx::tma_prefetch_desc(&tmQ);
@@ -141,25 +150,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = ptx::idesc_f16(128, 128, false);   // fp16 Qr x fp16 Kr
-      constexpr uint32_t idO = ptx::idesc_bf16(128, 64, true);   // bf16 P x bf16 V
-      const uint32_t q_base = ptx::smem_addr(sm.q[0]);
+      constexpr uint32_t idS = ptx::idesc_f16(128, 128, false);  // fp16 Qr x fp16 Kr
+      constexpr uint32_t idO = ptx::idesc_f16(128, 80, true);    // fp16 P x [fp16 V | ones]
+      // Descriptors are built once; per MMA only a small constant is added to
+      // the address field (16-byte units): +2 per 16-element K step of a
+      // K-major operand, +128 per 16-key step of the MN-major V operand, and
+      // 1024 per 16 KiB tile.
+      constexpr uint64_t kTileStep = kTileBytes >> 4;
+      const uint64_t dq = desc_k_major(ptx::smem_addr(sm.q[0]));
+      const uint64_t dk = desc_k_major(ptx::smem_addr(sm.k[0]));
+      // V stage st: the ones atom is (kStages - st) tiles further on (LBO)
+      uint64_t dv[kStages];
+#pragma unroll
+      for (int st = 0; st < kStages; ++st)
+        dv[st] = ptx::sdesc_sw128(ptx::smem_addr(sm.v[st]), (kStages - st) * kTileBytes);
       auto issue_s = [&](int i, int st) {
-        const uint32_t kb = ptx::smem_addr(sm.k[st]), qb = q_base + i * kTileBytes;
+        const uint64_t a0 = dq + i * kTileStep, b0 = dk + st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f16_ss(tmem + 128 * i, desc_k_major(qb + 32 * kk), desc_k_major(kb + 32 * kk),
-                          idS, kk > 0);
+          ptx::mma_f16_ss(tmem + 128 * i, a0 + 2 * kk, b0 + 2 * kk, idS, kk > 0);
         ptx::mma_commit(&sm.bar_s[i]);
       };
-      auto issue_o = [&](int i, int st, bool acc) {
-        const uint32_t vb = ptx::smem_addr(sm.v[st]);
-        const uint32_t pb = ptx::smem_addr(sm.p[i][0]);
+      auto issue_o = [&](int i, uint64_t vdesc, bool acc) {
+        // P_i: 128 keys as 64 packed columns at the start of S_i, 8 per K step
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_f16_ss(tmem + 256 + 64 * i,
-                          desc_k_major(pb + (kk >> 2) * kTileBytes + 32 * (kk & 3)),
-                          desc_mn_major(vb + 2048 * kk), idO, (acc || kk > 0) ? 1u : 0u);
+          ptx::mma_f16_ts(tmem + 256 + 80 * i, tmem + 128 * i + 8 * kk, vdesc + 128 * kk, idO,
+                          (acc || kk > 0) ? 1u : 0u);
         ptx::mma_commit(&sm.bar_o[i]);
       };
       wait_bar(&sm.bar_q, 0, p.status);
@@ -171,9 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = n % kStages;
         const int st1 = (n + 1) % kStages;
         wait_bar(&sm.bar_v[st], (n / kStages) & 1, p.status);
+        static_assert(kStages == 3, "stage descriptor selection");
+        const uint64_t vdesc = st == 0 ? dv[0] : (st == 1 ? dv[1] : dv[2]);
         wait_bar(&sm.bar_p[0], n & 1, p.status);
         ptx::tc_fence_after();
-        issue_o(0, st, n > 0);
+        issue_o(0, vdesc, n > 0);
         if (n + 1 < n_win) {
           wait_bar(&sm.bar_k[st1], ((n + 1) / kStages) & 1, p.status);
           ptx::tc_fence_after();
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         wait_bar(&sm.bar_p[1], n & 1, p.status);
         ptx::tc_fence_after();
-        issue_o(1, st, n > 0);
+        issue_o(1, vdesc, n > 0);
         if (n + 1 < n_win) issue_s(1, st1);
         ptx::mma_commit(&sm.bar_empty[st]);
       }
@@ -197,11 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = p.tok_seg[valid ? t : qt.t0];
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + i * 128;
-    const uint32_t tO = tmem + lane_base + 256 + i * 64;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t tO = tmem + lane_base + 256 + i * 80;
+    const uint32_t tL = tO + 64;  // row sums
+    const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
+    float m_run = -INFINITY;
     int n_partial = 0;
+    uint32_t win = p.windows[qt.win_off];
     for (int n = 0; n < n_win; ++n) {
-      const uint32_t win = p.windows[qt.win_off + n];
+      const uint32_t win_next = n + 1 < n_win ? p.windows[qt.win_off + n + 1] : 0u;
       const bool full = (win & kWinFull) != 0;
       // visibility bits of this row over the window's 128 keys
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
@@ -222,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vis[w] = bits;
         }
       }
+      win = win_next;
       wait_bar(&sm.bar_s[i], n & 1, p.status);
       ptx::tc_fence_after();
       uint32_t sr[128];
@@ -235,9 +258,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (!((vis[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
       }
-      float mx = __uint_as_float(sr[0]);
+      // row max: eight independent 3-input chains, then a short tree
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      for (int k8 = 0; k8 < 8; ++k8) mx8[k8] = __uint_as_float(sr[k8]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 16)
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8)
+          mx8[k8] = ptx::max3(mx8[k8], __uint_as_float(sr[c + k8]), __uint_as_float(sr[c + 8 + k8]));
+      const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
+                             fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx * kScaleLog2);
       const bool need = m_new > m_run + kRescaleThreshold;
       const bool any = __any_sync(0xffffffffu, need);
@@ -247,26 +278,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
       const float mref = m_run == -INFINITY ? 0.f : m_run;
-      // P(n) overwrites P(n-1): PV(n-1) was issued before S(n), so it has
-      // completed by now and this wait returns at once
-      if (n > 0) wait_bar(&sm.bar_o[i], (n - 1) & 1, p.status);
-      float ls = 0.f;
+      const float2 neg2 = make_float2(-mref, -mref);
+      // p = 2^(s * scale - m): packed fp32 FMA, then a packed fp16 exp whose
+      // result is already the fp16 A operand of the P x V product.  Word k of
+      // the row holds keys 2k, 2k+1 and overwrites S column k (already read).
+      uint32_t pw[64];
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[8 * ch + 2 * e]), kScaleLog2, -mref));
-          const float p1 =
-              ptx::ex2(fmaf(__uint_as_float(sr[8 * ch + 2 * e + 1]), kScaleLog2, -mref));
-          ls += p0 + p1;
-          w4[e] = pack_bf16(p0, p1);
-        }
-        const int c = ch & 7;
-        uint8_t *dst = sm.p[i][ch >> 3] + row * 128 + ((c ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      for (int k2 = 0; k2 < 64; ++k2) {
+        const float2 sv = make_float2(__uint_as_float(sr[2 * k2]), __uint_as_float(sr[2 * k2 + 1]));
+        const float2 x = __ffma2_rn(sv, scale2, neg2);
+        __half2 h = __floats2half2_rn(x.x, x.y);
+        pw[k2] = ptx::ex2_f16x2(*reinterpret_cast<uint32_t *>(&h));
       }
-      l_run = l_run * alpha + ls;
+      ptx::tmem_st32(tS, pw);
+      ptx::tmem_st32(tS + 32, pw + 32);
+      // O may be rescaled only once PV(n-1) has completed; PV(n-1) was issued
+      // before S(n), so it has, and this wait returns at once
+      if (n > 0) wait_bar(&sm.bar_o[i], (n - 1) & 1, p.status);
       if (n > 0 && any) {  // rare: the running max grew by more than 2^8
         ptx::tc_fence_after();
 #pragma unroll
@@ -279,22 +307,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           ptx::tmem_st32(tO + 32 * hlf, o);
         }
-        ptx::tmem_wait_st();
+        uint32_t lsum[16];
+        ptx::tmem_ld16(tL, lsum);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence16(lsum);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) lsum[c] = __float_as_uint(__uint_as_float(lsum[c]) * alpha);
+        ptx::tmem_st16(tL, lsum);
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.bar_p[i]);
     }
     wait_bar(&sm.bar_o[i], (n_win - 1) & 1, p.status);
     ptx::tc_fence_after();
-    uint32_t o[64];
+    uint32_t o[64], lsum[16];
     ptx::tmem_ld32(tO, o);
     ptx::tmem_ld32(tO + 32, o + 32);
+    ptx::tmem_ld16(tL, lsum);
     ptx::tmem_wait_ld();
     ptx::reg_fence32(o);
     ptx::reg_fence32(o + 32);
+    ptx::reg_fence16(lsum);
     if (valid) {
-      const float inv = 1.f / l_run;
+      const float inv = 1.f / __uint_as_float(lsum[0]);
       uint4 *dst = reinterpret_cast<uint4 *>(out + ((int64_t)t * p.Hq + h0 + i) * kD);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -354,7 +390,7 @@ cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, p.qr, (int64_t)p.Hq * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
       !make_map(&mk, p.kr, (int64_t)p.max_ver * p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
-      !make_map(&mv, p.vp, (int64_t)p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      !make_map(&mv, p.vp, (int64_t)p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return cudaErrorInvalidValue;
   const int smem = (int)sizeof(Smem) + 1024;
   static bool attr = false;

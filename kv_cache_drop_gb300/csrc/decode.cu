@@ -107,7 +107,10 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // Q fragments (A operand, rows = query heads of the group, 16 rows padded
   // with zeros), rotated at the query position; 1/sqrt(D) * log2(e) folded in.
-  uint32_t qa[4][4];
+  // The rotated query is not a bf16 value: it is split into hi + lo bf16
+  // parts (hi = bf16(q), lo = bf16(q - hi)) and S = hi K^T + lo K^T, so the
+  // scores carry ~16 mantissa bits of q at twice the (idle) MMA work.
+  uint32_t qa[4][4], ql[4][4];
   {
     const float qs = 0.125f * kLog2e;
     float qv[2][16];  // [row half][element]: rows gid and gid+8
@@ -137,12 +140,18 @@ __global__ void __launch_bounds__(kWarps * 32)
           qv[hh][ks * 4 + e] = (x1 * cs[d] - x2 * sn[d]) * qs;
           qv[hh][(ks + 2) * 4 + e] = (x1 * sn[d] + x2 * cs[d]) * qs;
         }
+    auto lo = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      qa[ks][0] = pack_bf16(qv[0][ks * 4 + 0], qv[0][ks * 4 + 1]);
-      qa[ks][1] = pack_bf16(qv[1][ks * 4 + 0], qv[1][ks * 4 + 1]);
-      qa[ks][2] = pack_bf16(qv[0][ks * 4 + 2], qv[0][ks * 4 + 3]);
-      qa[ks][3] = pack_bf16(qv[1][ks * 4 + 2], qv[1][ks * 4 + 3]);
+      const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
+      qa[ks][0] = pack_bf16(a0[0], a0[1]);
+      qa[ks][1] = pack_bf16(a1[0], a1[1]);
+      qa[ks][2] = pack_bf16(a0[2], a0[3]);
+      qa[ks][3] = pack_bf16(a1[2], a1[3]);
+      ql[ks][0] = pack_bf16(lo(a0[0]), lo(a0[1]));
+      ql[ks][1] = pack_bf16(lo(a1[0]), lo(a1[1]));
+      ql[ks][2] = pack_bf16(lo(a0[2]), lo(a0[3]));
+      ql[ks][3] = pack_bf16(lo(a1[2]), lo(a1[3]));
     }
   }
 
@@ -198,6 +207,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       ldsm_x4(kt + swz(key, ch), b00, b01, b10, b11);
       mma_bf16(s[0], qa[ks], b00, b01);
       mma_bf16(s[1], qa[ks], b10, b11);
+      mma_bf16(s[0], ql[ks], b00, b01);
+      mma_bf16(s[1], ql[ks], b10, b11);
     }
     // mask the ragged tail; online softmax in log2 units
     float mx[2] = {-INFINITY, -INFINITY};

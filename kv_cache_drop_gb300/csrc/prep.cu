@@ -6,14 +6,17 @@
 //                                                  slots in the plan's order
 //  * Vp[g][j]     = V[src(j)][g]                  values copied once, shared
 //                                                  by every version
-// For bf16 inputs the rotated copies Qr and Kr are written as fp16: the
-// rotation's output is not a bf16 value anyway, and fp16 keeps 3 more
-// mantissa bits for the score contraction at the same tensor-core rate.
-// An output beyond the fp16 range sets status bit kStatusFp16Range.
+// For bf16 inputs all three copies are written as fp16: the rotation's output
+// is not a bf16 value anyway, fp16 keeps 3 more mantissa bits for the score
+// contraction at the same tensor-core rate, and fp16 V lets the softmax hand
+// fp16 probabilities (packed fp16 exp) straight to the P x V product.  A
+// value beyond the fp16 range sets status bit kStatusFp16Range.
 // Outputs are head-major so that a 128-row tile of one head is 16 KiB of
 // contiguous memory (one TMA box).  Each CTA takes 32 rows, computes their
 // 32 x 32 cos/sin table once in shared memory, and streams 16-byte chunks.
 #include "common.cuh"
+
+#include <type_traits>
 
 namespace akv {
 namespace {
@@ -85,8 +88,22 @@ __global__ void __launch_bounds__(kThreads) prep_kv_kernel(PlanDev p, const T *_
       const int64_t j = j0 + r;
       if (j >= p.T) continue;
       const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + ((int64_t)src[r] * p.Hkv + g) * kD) + c);
-      reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.vp) + ((int64_t)g * p.T + j) * kD)[c] = x;
+      uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<TR *>(p.vp) + ((int64_t)g * p.T + j) * kD) + c;
+      if constexpr (sizeof(TR) == sizeof(T)) {
+        if constexpr (std::is_same<TR, T>::value) {
+          *dst = x;
+        } else {  // bf16 -> fp16
+          float f[E];
+          chunk_to_f32<T>(x, f);
+          float big = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) big = fmaxf(big, fabsf(f[e]));
+          ovf |= !(big <= 65504.f);
+          *dst = f32_to_chunk<TR>(f);
+        }
+      }
     }
+    if (sizeof(TR) == 2 && ovf) atomicOr(p.status, kStatusFp16Range);
   }
 }
 

@@ -8,6 +8,12 @@ import oracle
 BF16_MAX_ABS = 2e-2        # bf16 inputs, fp32 accumulation
 BF16_REL_RMS = 2.0 ** -7   # error RMS / reference RMS
 F32_MAX_ABS = 1e-4
+# Queries scaled by 8 (score std ~8): scores are formed from fp16 copies of
+# the rotated Q and K (relative rounding 2^-11 each) and the output is rounded
+# to bf16; a score of ~3 sigma = 24 then moves by ~24 * 2 * 2^-11 = 0.02 nat,
+# a softmax weight by ~2% and the output by up to ~0.03, plus <= 0.008 of bf16
+# output rounding: max-abs 4e-2.
+BF16_PEAKY_MAX_ABS = 4e-2
 
 
 def run_prefill(reqs, device="cuda"):
@@ -52,11 +58,11 @@ def err(got, ref):
     return float(d.max()), float(np.sqrt(np.mean(d * d)) / rms_ref)
 
 
-def assert_close(got, ref, dtype):
+def assert_close(got, ref, dtype, max_abs=None):
     mx, rel = err(got, ref)
     print(f"[parity] {dtype} max_abs={mx:.3e} rel_rms={rel:.3e}")
     if dtype == "bf16":
-        assert mx <= BF16_MAX_ABS and rel <= BF16_REL_RMS, (mx, rel)
+        assert mx <= (max_abs or BF16_MAX_ABS) and rel <= BF16_REL_RMS, (mx, rel)
     else:
         assert mx <= F32_MAX_ABS, (mx, rel)
     return mx, rel
