@@ -292,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_st32(tS, pw);
       ptx::tmem_st32(tS + 32, pw + 32);
-      // O may be rescaled only once PV(n-1) has completed; PV(n-1) was issued
-      // before S(n), so it has, and this wait returns at once
-      if (n > 0) wait_bar(&sm.bar_o[i], (n - 1) & 1, p.status);
       if (n > 0 && any) {  // rare: the running max grew by more than 2^8
+        // O may be rescaled only once PV(n-1) has completed; PV(n-1) was
+        // issued before S(n), so this wait returns at once
+        wait_bar(&sm.bar_o[i], (n - 1) & 1, p.status);
         ptx::tc_fence_after();
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
