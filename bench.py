@@ -233,11 +233,13 @@ def repos_part(traj, steps, warmup):
     r = akv.akv_compact(traj.ops(), T, b, idx, pos, cws)
     ko = torch.empty((r, traj.Hkv, 64), dtype=k.dtype, device="cuda")
     vo = torch.empty_like(ko)
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    flush = torch.ones(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     t_c, t_r = [], []
     for it in range(warmup + steps):
-        flush.zero_()  # L2 flush: the survivors (~115 MB) would otherwise sit in L2
+        # L2 flush: the survivors (~107 MB) would otherwise sit in L2.  A read
+        # pass leaves clean lines, so no write-back is charged to the kernel.
+        flush_sum = flush.sum()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record(stream)
         akv.akv_compact(traj.ops(), T, b, idx, pos, cws)
@@ -252,10 +254,27 @@ def repos_part(traj, steps, warmup):
     bytes_rot = r * (4 * row + 8)  # K, V read + written; src index and position read
     ms_r = float(np.mean(t_r))
     ms_c = float(np.mean(t_c))
-    del k, v, ko, vo, flush
+    # what one launch moving the same number of bytes reaches on this GPU: a
+    # plain contiguous device copy of K+V of the survivors, same flush
+    src = torch.empty(r * 2 * traj.Hkv * 64, dtype=k.dtype, device="cuda")
+    dst = torch.empty_like(src)
+    t_cp = []
+    for it in range(warmup + steps):
+        flush_sum = flush.sum()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        dst.copy_(src)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        if it >= warmup:
+            t_cp.append(e[0].elapsed_time(e[1]))
+    ms_cp = float(np.mean(t_cp))
+    del k, v, ko, vo, flush, src, dst
     torch.cuda.empty_cache()
     return dict(r=int(r), rotate_ms=ms_r, compact_ms=ms_c, bytes=int(bytes_rot),
                 rotate_gbs=bytes_rot / ms_r / 1e6,
+                same_size_copy_gbs=(4 * r * row) / ms_cp / 1e6,
+                frac_of_same_size_copy=(bytes_rot / ms_r) / ((4 * r * row) / ms_cp),
                 compact_plus_rotate_gbs=(bytes_rot + 8 * T) / (ms_r + ms_c) / 1e6)
 
 
@@ -333,6 +352,12 @@ def run_ours(args, rank, world):
     import workloads
     akv.lib()
     pk = peaks()
+    if args.part in ("repos", "decode"):  # one secondary workload alone (profiling captures)
+        if args.part == "repos":
+            res = repos_part(workloads.repos_config(), args.steps, args.warmup)
+        else:
+            res = decode_part(workloads.decode_workload())
+        return {"part": args.part, **res}
     traj = workloads.rolling_drop_config(rounds=args.rounds)
     main = prefill_part(traj, args.steps, args.warmup, world, with_e2e=not args.no_e2e)
     steps = args.steps
@@ -442,6 +467,8 @@ def main():
                     help="agent rounds of the headline trajectory (100 = the benchmark "
                          "workload; fewer only for small profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--part", default="all", choices=["all", "repos", "decode"],
+                    help="run one secondary workload alone (for profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

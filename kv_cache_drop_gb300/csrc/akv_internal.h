@@ -56,9 +56,12 @@ struct PlanDev {
   int32_t dtype;             // akv_dtype
 };
 
-// RoPE frequencies theta_i = base^(-2i/D), computed in double on the host.
+// RoPE frequencies theta_i = base^(-2i/D), computed in double on the host,
+// also as an unevaluated float pair hi + lo (hi = fl(theta), lo = fl(theta - hi)).
 struct RopeTheta {
   double th[kD / 2];
+  float hi[kD / 2];
+  float lo[kD / 2];
 };
 
 void rope_theta(float base, RopeTheta *out);

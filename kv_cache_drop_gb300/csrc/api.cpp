@@ -113,7 +113,11 @@ akv_status check_oplog(const akv_oplog *o, int64_t T, int req) {
 }  // namespace
 
 void akv::rope_theta(float base, RopeTheta *out) {
-  for (int i = 0; i < kD / 2; ++i) out->th[i] = std::pow((double)base, -2.0 * i / kD);
+  for (int i = 0; i < kD / 2; ++i) {
+    out->th[i] = std::pow((double)base, -2.0 * i / kD);
+    out->hi[i] = (float)out->th[i];
+    out->lo[i] = (float)(out->th[i] - (double)out->hi[i]);
+  }
 }
 
 // ------------------------------------------------------------------------

@@ -21,6 +21,29 @@ __device__ __forceinline__ void rope_cs(double theta, double pos, float *c, floa
   sincosf(r, s, c);
 }
 
+// cos/sin of pos * theta_i without fp64 arithmetic for |pos| <= 2^18.
+// The product pos * (hi + lo) is kept as an unevaluated float sum (the
+// rounding error of pos * hi recovered exactly with an FMA, Dekker), and it is
+// reduced by 2*pi split into three floats, the first two with 8 significant
+// bits so that k * C1 and k * C2 are exact for |k| < 2^16 (Cody-Waite).  The
+// reduced angle is accurate to ~3e-7 rad.  Larger positions take the double
+// path above.
+__device__ __forceinline__ void rope_cs(const RopeTheta &th, int f, int pos, float *c, float *s) {
+  if (pos < -262144 || pos > 262144) {
+    rope_cs(th.th[f], (double)pos, c, s);
+    return;
+  }
+  const float p = (float)pos;  // exact
+  const float ah = p * th.hi[f];
+  const float ae = fmaf(p, th.hi[f], -ah);  // exact error of the product
+  const float al = fmaf(p, th.lo[f], ae);
+  const float k = rintf(ah * 0.159154943091895336f);
+  float r = fmaf(-k, 6.28125f, ah);            // 2*pi = 6.28125
+  r = fmaf(-k, 1.93023681640625e-3f, r);       //      + 1.93023681640625e-3
+  r = fmaf(-k, 5.0703633860393888e-6f, r);     //      + 5.07036338...e-6 (+ ~2e-13)
+  sincosf(r + al, s, c);
+}
+
 // 16-byte chunks of one head row (D = 64): a bf16 chunk holds 8 elements, an
 // f32 chunk 4.  Pair (i, i + D/2) lives in chunks c and c + kHalfChunks.
 template <typename T>

@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) prep_q_kernel(PlanDev p, const T *__
   const int64_t t0 = (int64_t)blockIdx.x * kRows;
   for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
     const int r = i / (kD / 2), f = i % (kD / 2);
-    if (t0 + r < p.T) rope_cs(th.th[f], (double)p.tok_qpos[t0 + r], &cs[r][f], &sn[r][f]);
+    if (t0 + r < p.T) rope_cs(th, f, p.tok_qpos[t0 + r], &cs[r][f], &sn[r][f]);
   }
   __syncthreads();
   const int units = kRows * p.Hq * H;
@@ -64,8 +64,7 @@ __global__ void __launch_bounds__(kThreads) prep_kv_kernel(PlanDev p, const T *_
     for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
       const int r = i / (kD / 2), f = i % (kD / 2);
       if (j0 + r < p.T)
-        rope_cs(th.th[f], (double)p.slot_pos[(int64_t)plane * p.T + j0 + r], &cs[r][f],
-                &sn[r][f]);
+        rope_cs(th, f, p.slot_pos[(int64_t)plane * p.T + j0 + r], &cs[r][f], &sn[r][f]);
     }
   }
   __syncthreads();

@@ -41,8 +41,8 @@ __global__ void __launch_bounds__(kThreads)
     const int r = i / (kD / 2), f = i % (kD / 2);
     const int j = j0 + r;
     if (j < n) {
-      const double delta = kScatter ? (double)pf[j] : (double)((pt ? pt[j] : j) - pf[j]);
-      rope_cs(th.th[f], delta, &cs[r][f], &sn[r][f]);
+      const int delta = kScatter ? pf[j] : (pt ? pt[j] : j) - pf[j];
+      rope_cs(th, f, delta, &cs[r][f], &sn[r][f]);
     }
   }
   __syncthreads();

@@ -227,3 +227,27 @@ def test_errors_are_reported_before_launch():
         p2 = akv.Plan(akv.shape(6, 2, 64, "bf16"), [0, r.T], [r.ops()])
         akv.akv_segment_attention_run(p2, q, k, v, torch.empty_like(q), p2.workspace())
     assert e.value.status == 4  # odd query heads per KV head in bf16
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_append_rotation_across_position_ranges(dtype):
+    """Positions on both sides of the fp32 angle-reduction range (|pos| <= 2^18)
+    and far beyond it rotate like the fp64 oracle."""
+    torch = _torch()
+    pos = np.array([0, 1, 4095, 131071, 262143, 262144, 262145, 300000, 1 << 20, (1 << 24) + 3,
+                    (1 << 30) + 7, 2**31 - 1], dtype=np.int64)
+    n = len(pos)
+    rng = np.random.default_rng(12)
+    k = workloads.gen._normals(rng, (n, 4, 64), dtype)
+    v = workloads.gen._normals(rng, (n, 4, 64), dtype)
+    shp = akv.shape(8, 4, 64, dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kp = torch.zeros((n, 4, 64), dtype=tdt, device="cuda")
+    vp = torch.zeros_like(kp)
+    akv.akv_append_kv(shp, n, akv.to_device(k, dtype), akv.to_device(v, dtype),
+                      akv.i32_device(pos), akv.i32_device(np.arange(n)[::-1].copy()), kp, vp)
+    torch.cuda.synchronize()
+    ref = oracle.rope(oracle.widen(k, dtype), pos[:, None], 10000.0)[::-1]
+    tol = 2 ** -8 * 4 if dtype == "bf16" else 2e-5
+    assert np.max(np.abs(kp.float().cpu().numpy() - ref)) <= tol
+    assert np.array_equal(vp.float().cpu().numpy(), oracle.widen(v, dtype)[::-1])
