@@ -251,6 +251,48 @@ akv_status akv_append_kv(const akv_shape *shape, int32_t n, const void *k_new, c
                          const int32_t *pos, const int32_t *slot, void *k_pool, void *v_pool,
                          akv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Decoder layers of a single-prefill restoration (paper review page section
+ * 4.2, Appendix A.1.1, Figure 10): attention is cut into segments, every
+ * other layer op (projections, FFN) runs once over the whole batched
+ * sequence.  Pre-norm layer: a = RMSNorm(h); q,k,v = a Wq^T, a Wk^T, a Wv^T;
+ * h += SegmentAttention(q,k,v) Wo^T; f = RMSNorm(h);
+ * h += (silu(f Wg^T) * (f Wu^T)) Wd^T.  The residual stream h is fp32.
+ * ---------------------------------------------------------------------- */
+
+/* Y[M,N] (+)= X[M,K] * W[N,K]^T on the tensor cores.  x: device bf16 [M,K];
+ * w: device bf16 [N,K] (row n = output feature n); y: device, out_mode 0 =
+ * bf16 [M,N] store, 1 = fp32 store, 2 = fp32 y += product.  N % 32 == 0,
+ * K % 8 == 0, pointers 16-byte aligned. */
+akv_status akv_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *x, const void *w, void *y,
+                         int32_t out_mode, akv_stream_t stream);
+
+/* y[r] = x[r] / sqrt(mean(x[r]^2) + eps) * weight (weight NULL = ones).
+ * x, y: device [rows, d] of the given dtypes; weight: device fp32 [d]. */
+akv_status akv_rmsnorm(int32_t rows, int32_t d, float eps, akv_dtype in_dtype, const void *x,
+                       const float *weight, akv_dtype out_dtype, void *y, akv_stream_t stream);
+
+/* out = silu(g) * u element-wise, bf16 [n]; out may equal g. */
+akv_status akv_swiglu(int64_t n, const void *g, const void *u, void *out, akv_stream_t stream);
+
+/* Weights of one layer, device bf16, each [out_features][in_features]:
+ * wq [Hq*D][d], wk and wv [Hkv*D][d], wo [d][Hq*D], wg and wu [d_ff][d],
+ * wd [d][d_ff]. */
+typedef struct {
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+} akv_layer_weights;
+
+/* n_layers decoder layers over the planned batch (plan: bf16, its op logs
+ * shape every layer's attention the same way), then a final RMSNorm.
+ * layers: host array [n_layers]; x: device bf16 [T, d_model] embeddings;
+ * out: device fp32 [T, d_model].  workspace >= akv_decoder_workspace();
+ * it starts with the status word read by akv_workspace_status. */
+size_t akv_decoder_workspace(const akv_plan *plan, int32_t d_model, int32_t d_ff);
+akv_status akv_decoder_forward(const akv_plan *plan, int32_t n_layers,
+                               const akv_layer_weights *layers, int32_t d_model, int32_t d_ff,
+                               float eps, const void *x, float *out, void *workspace,
+                               size_t workspace_bytes, akv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

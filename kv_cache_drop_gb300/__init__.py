@@ -57,6 +57,10 @@ class PlanInfo(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd")]
+
+
 _lib = None
 
 _SIGS = {
@@ -99,6 +103,17 @@ _SIGS = {
                                     [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_void_p,
                                                              ctypes.c_void_p]),
     "akv_decode_static_scratch_bytes": (ctypes.c_size_t, []),
+    "akv_gemm_bf16": (ctypes.c_int, [ctypes.c_int32] * 3 + [ctypes.c_void_p] * 3 +
+                      [ctypes.c_int32, ctypes.c_void_p]),
+    "akv_rmsnorm": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                   ctypes.c_void_p, ctypes.c_void_p]),
+    "akv_swiglu": (ctypes.c_int, [ctypes.c_int64] + [ctypes.c_void_p] * 4),
+    "akv_decoder_workspace": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
+    "akv_decoder_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.POINTER(LayerWeights), ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_float] +
+                            [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
     "akv_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
                       [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),
 }
@@ -330,3 +345,34 @@ def to_device(arr: np.ndarray, dtype: str, device="cuda"):
 def i32_device(a, device="cuda"):
     import torch
     return torch.from_numpy(_i32(a)).to(device)
+
+
+def akv_gemm_bf16(M: int, N: int, K: int, x, w, y, out_mode: int = 0, stream=None):
+    _check(lib().akv_gemm_bf16(M, N, K, _dev(x), _dev(w), _dev(y), out_mode, _stream(stream)))
+
+
+def akv_rmsnorm(rows: int, d: int, eps: float, x, y, weight=None, stream=None):
+    import torch
+    code = {torch.float32: AKV_F32, torch.bfloat16: AKV_BF16}
+    _check(lib().akv_rmsnorm(rows, d, eps, code[x.dtype], _dev(x), _dev(weight), code[y.dtype],
+                             _dev(y), _stream(stream)))
+
+
+def akv_swiglu(n: int, g, u, out, stream=None):
+    _check(lib().akv_swiglu(n, _dev(g), _dev(u), _dev(out), _stream(stream)))
+
+
+def akv_decoder_workspace(plan: Plan, d_model: int, d_ff: int) -> int:
+    return lib().akv_decoder_workspace(plan.handle, d_model, d_ff)
+
+
+def akv_decoder_forward(plan: Plan, layers, d_model: int, d_ff: int, eps: float, x, out,
+                        workspace, stream=None):
+    """layers: list of dicts of device bf16 tensors wq..wd, each [out, in]."""
+    arr = (LayerWeights * max(1, len(layers)))()
+    for i, w in enumerate(layers):
+        arr[i] = LayerWeights(*[w[n].data_ptr() for n in ("wq", "wk", "wv", "wo", "wg", "wu",
+                                                          "wd")])
+    _check(lib().akv_decoder_forward(plan.handle, len(layers), arr, d_model, d_ff, eps, _dev(x),
+                                     _dev(out), _dev(workspace), workspace.numel(),
+                                     _stream(stream)))

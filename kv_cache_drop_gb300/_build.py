@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libakv.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 SOURCES = ["api.cpp", "prep.cu", "attn_simt.cu", "attn_tc.cu", "repos.cu", "compact.cu",
-           "decode.cu"]
+           "decode.cu", "gemm.cu", "norm.cu"]
 
 
 def _nvcc() -> str:

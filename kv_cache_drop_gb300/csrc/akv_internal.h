@@ -100,6 +100,14 @@ cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, cons
                           const int32_t *indices, int max_kv, void *out, void *ws,
                           const RopeTheta &th, cudaStream_t s);
 
+// Decoder-layer pieces (GEMM: out_mode 0 bf16, 1 fp32, 2 fp32 +=)
+cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void *y, int out_mode,
+                        uint32_t *status, cudaStream_t s);
+cudaError_t launch_rmsnorm(int rows, int d, float eps, int in_f32, const void *x, const float *w,
+                           int out_f32, void *y, cudaStream_t s);
+cudaError_t launch_swiglu(int64_t n, const void *g, const void *u, void *out, cudaStream_t s);
+cudaError_t launch_widen(int64_t n, const void *x, float *y, cudaStream_t s);
+
 // Decode with its split-KV partials in a static device array (no workspace).
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 cudaError_t decode_static_scratch(void **ptr);

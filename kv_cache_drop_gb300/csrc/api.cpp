@@ -771,4 +771,136 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
 
 size_t akv_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
+// ------------------------------------------------------------------------
+// Decoder layers around the segment attention
+// ------------------------------------------------------------------------
+
+akv_status akv_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *x, const void *w, void *y,
+                         int32_t out_mode, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_gemm_bf16")) return f;
+  if (M < 0 || N < 0 || K <= 0 || out_mode < 0 || out_mode > 2)
+    return fail(AKV_ERR_INVALID, "bad GEMM arguments");
+  if (N % 32 || K % 8)
+    return fail(AKV_ERR_UNSUPPORTED, "GEMM needs N %% 32 == 0 and K %% 8 == 0 (N=%d K=%d)", N, K);
+  if ((int64_t)M * 1 >= (int64_t)1 << 31) return fail(AKV_ERR_UNSUPPORTED, "M too large");
+  if (M == 0 || N == 0) return AKV_OK;
+  if (!x || !w || !y) return fail(AKV_ERR_INVALID, "NULL argument");
+  if ((uintptr_t)x % 16 || (uintptr_t)w % 16 || (uintptr_t)y % 16)
+    return fail(AKV_ERR_INVALID, "GEMM operands must be 16-byte aligned");
+  cudaError_t e = launch_gemm(M, N, K, x, w, y, out_mode, nullptr, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm");
+  return AKV_OK;
+}
+
+akv_status akv_rmsnorm(int32_t rows, int32_t d, float eps, akv_dtype in_dtype, const void *x,
+                       const float *weight, akv_dtype out_dtype, void *y, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_rmsnorm")) return f;
+  if (rows < 0 || d <= 0 || !(eps >= 0.f)) return fail(AKV_ERR_INVALID, "bad rmsnorm arguments");
+  if (rows == 0) return AKV_OK;
+  if (!x || !y) return fail(AKV_ERR_INVALID, "NULL argument");
+  cudaError_t e = launch_rmsnorm(rows, d, eps, in_dtype == AKV_F32, x, weight, out_dtype == AKV_F32,
+                                 y, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm");
+  return AKV_OK;
+}
+
+akv_status akv_swiglu(int64_t n, const void *g, const void *u, void *out, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_swiglu")) return f;
+  if (n < 0) return fail(AKV_ERR_INVALID, "n < 0");
+  if (n == 0) return AKV_OK;
+  if (!g || !u || !out) return fail(AKV_ERR_INVALID, "NULL argument");
+  cudaError_t e = launch_swiglu(n, g, u, out, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "swiglu");
+  return AKV_OK;
+}
+
+namespace {
+struct DecoderLayout {
+  size_t h, a, q, k, v, o, g, u, attn, total;
+};
+DecoderLayout decoder_layout(const akv_plan *P, int d_model, int d_ff) {
+  DecoderLayout L{};
+  const size_t T = (size_t)P->T;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    off = align_up(off, 1024);
+    size_t r = off;
+    off += bytes;
+    return r;
+  };
+  L.attn = take(P->ws.total);  // first: its status word starts the workspace
+  L.h = take(4 * T * d_model);
+  L.a = take(2 * T * d_model);
+  L.q = take(2 * T * P->shape.Hq * kD);
+  L.k = take(2 * T * P->shape.Hkv * kD);
+  L.v = take(2 * T * P->shape.Hkv * kD);
+  L.o = take(2 * T * P->shape.Hq * kD);
+  L.g = take(2 * T * d_ff);
+  L.u = take(2 * T * d_ff);
+  L.total = align_up(off, 1024);
+  return L;
+}
+}  // namespace
+
+size_t akv_decoder_workspace(const akv_plan *P, int32_t d_model, int32_t d_ff) {
+  if (!P || d_model <= 0 || d_ff <= 0) return 0;
+  return decoder_layout(P, d_model, d_ff).total;
+}
+
+akv_status akv_decoder_forward(const akv_plan *P, int32_t n_layers, const akv_layer_weights *layers,
+                               int32_t d_model, int32_t d_ff, float eps, const void *x, float *out,
+                               void *workspace, size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_decoder_forward")) return f;
+  if (!P || n_layers < 0 || (n_layers > 0 && !layers) || d_model <= 0 || d_ff <= 0 || !x || !out)
+    return fail(AKV_ERR_INVALID, "bad decoder arguments");
+  if (P->shape.dtype != AKV_BF16) return fail(AKV_ERR_UNSUPPORTED, "decoder layers run in bf16");
+  if (d_model % 32 || d_ff % 32)
+    return fail(AKV_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 32");
+  for (int l = 0; l < n_layers; ++l) {
+    const akv_layer_weights &w = layers[l];
+    if (!w.wq || !w.wk || !w.wv || !w.wo || !w.wg || !w.wu || !w.wd)
+      return fail(AKV_ERR_INVALID, "layer %d: NULL weight", l);
+  }
+  const DecoderLayout L = decoder_layout(P, d_model, d_ff);
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < L.total)
+    return fail(AKV_ERR_WORKSPACE, "decoder workspace: need %zu aligned bytes", L.total);
+  if (P->T == 0) return AKV_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *b = (char *)workspace;
+  float *h = (float *)(b + L.h);
+  void *a = b + L.a, *q = b + L.q, *k = b + L.k, *v = b + L.v, *o = b + L.o, *g = b + L.g,
+       *u = b + L.u, *aws = b + L.attn;
+  const int T = (int)P->T, dq = P->shape.Hq * kD, dkv = P->shape.Hkv * kD;
+  uint32_t *status = (uint32_t *)((char *)aws + P->ws.status);
+  // The kernels' bounded waits stop waiting once this word is nonzero (a
+  // timeout elsewhere in the launch); a reused workspace may hold any value,
+  // so clear it before the first GEMM reads it.
+  cudaError_t e = cudaMemsetAsync(status, 0, 256, s);
+  if (e == cudaSuccess) e = launch_widen((int64_t)T * d_model, x, h, s);
+#define AKV_TRY(call, what)                       \
+  do {                                            \
+    if (e == cudaSuccess) e = (call);             \
+    if (e != cudaSuccess) return cuda_fail(e, what); \
+  } while (0)
+  AKV_TRY(cudaSuccess, "widen");
+  for (int l = 0; l < n_layers; ++l) {
+    const akv_layer_weights &w = layers[l];
+    AKV_TRY(launch_rmsnorm(T, d_model, eps, 1, h, nullptr, 0, a, s), "rmsnorm");
+    AKV_TRY(launch_gemm(T, dq, d_model, a, w.wq, q, 0, status, s), "q projection");
+    AKV_TRY(launch_gemm(T, dkv, d_model, a, w.wk, k, 0, status, s), "k projection");
+    AKV_TRY(launch_gemm(T, dkv, d_model, a, w.wv, v, 0, status, s), "v projection");
+    if (akv_status st = akv_segment_attention_run(P, q, k, v, o, aws, P->ws.total, stream))
+      return st;
+    AKV_TRY(launch_gemm(T, d_model, dq, o, w.wo, h, 2, status, s), "output projection");
+    AKV_TRY(launch_rmsnorm(T, d_model, eps, 1, h, nullptr, 0, a, s), "rmsnorm");
+    AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wg, g, 0, status, s), "gate projection");
+    AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wu, u, 0, status, s), "up projection");
+    AKV_TRY(launch_swiglu((int64_t)T * d_ff, g, u, g, s), "swiglu");
+    AKV_TRY(launch_gemm(T, d_model, d_ff, g, w.wd, h, 2, status, s), "down projection");
+  }
+  AKV_TRY(launch_rmsnorm(T, d_model, eps, 1, h, nullptr, 1, out, s), "final rmsnorm");
+#undef AKV_TRY
+  return AKV_OK;
+}
+
 }  // extern "C"

@@ -1,0 +1,196 @@
+// Projection / FFN GEMM of the restoration prefill's decoder layers (paper
+// review page section 4.2, Appendix A.1.1: attention is segmented, the FFN
+// runs once over the whole sequence):  Y[M,N] (+)= X[M,K] * W[N,K]^T.
+//
+// tcgen05 GEMM, one CTA per 128 x 256 output tile: warp 0 streams 64-wide K
+// blocks of X and W with TMA (128-byte swizzle) through a 4-stage ring, warp 1
+// allocates 256 TMEM columns and issues 128x256x16 MMAs from one thread,
+// warps 2-5 (one TMEM lane quarter each) read the fp32 accumulator back and
+// write bf16, fp32, or add into an fp32 output (the residual stream).
+// Waits are bounded like the attention kernel's.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <cuda.h>
+
+namespace akv {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2, kBBytes = BN * BK * 2;
+constexpr long long kWaitBudget = 1000000000LL;
+
+struct __align__(1024) GemmSmem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint64_t full[kStages], empty[kStages], done;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_t *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  if (status && *(volatile uint32_t *)status) return;
+  if (!ptx::mbar_wait(bar, parity, kWaitBudget) && status) atomicOr(status, kStatusWaitTimeout);
+}
+
+// out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add into Y
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                int M, int N, int K, void *__restrict__ Y, int out_mode, uint32_t *status) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem &sm = *reinterpret_cast<GemmSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int nk = (K + BK - 1) / BK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&sm.full[s], 1);
+      ptx::mbar_init(&sm.empty[s], 1);
+    }
+    ptx::mbar_init(&sm.done, 1);
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(&sm.tmem_base, BN);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmA);
+      ptx::tma_prefetch_desc(&tmB);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages) wait_bar(&sm.empty[s], ((kb / kStages) - 1) & 1, status);
+        ptx::mbar_expect_tx(&sm.full[s], kABytes + kBBytes);
+        ptx::tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * BK, m0);
+        ptx::tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * BK, n0);
+      }
+      for (int kb = nk > kStages ? nk - kStages : 0; kb < nk; ++kb)
+        wait_bar(&sm.full[kb % kStages], (kb / kStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id = ptx::idesc_bf16(BM, BN, false);
+      const uint64_t da = ptx::sdesc_sw128(ptx::smem_addr(sm.a[0]));
+      const uint64_t db = ptx::sdesc_sw128(ptx::smem_addr(sm.b[0]));
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        wait_bar(&sm.full[s], (kb / kStages) & 1, status);
+        ptx::tc_fence_after();
+        const uint64_t a0 = da + s * (kABytes >> 4), b0 = db + s * (kBBytes >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          ptx::mma_f16_ss(tmem, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(&sm.empty[s]);
+      }
+      ptx::mma_commit(&sm.done);
+    }
+  } else {
+    // epilogue: warp w owns TMEM lanes 32*(w%4) .. +31 = tile rows
+    const int row = 32 * (warp & 3) + lane;
+    const int m = m0 + row;
+    wait_bar(&sm.done, 0, status);
+    ptx::tc_fence_after();
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tl + c0, r);
+      ptx::tmem_wait_ld();
+      ptx::reg_fence32(r);
+      const int n = n0 + c0;
+      if (m >= M || n >= N) continue;  // N is a multiple of 32
+      if (out_mode == 0) {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * N + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * e]),
+                                                     __uint_as_float(r[8 * q + 2 * e + 1]));
+            w[e] = *reinterpret_cast<uint32_t *>(&h);
+          }
+          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(Y) + (int64_t)m * N + n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          if (out_mode == 2) {
+            const float4 o = dst[q];
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+          }
+          dst[q] = v;
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, BN);
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiled)f;
+  }
+  return fn;
+}
+
+// row-major [rows][K] bf16, box = box_rows x 64 (128-byte swizzle)
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void *y, int out_mode,
+                        uint32_t *status, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, x, M, K, BM) || !make_map(&mb, w, N, K, BN)) return cudaErrorInvalidValue;
+  const int smem = (int)sizeof(GemmSmem) + 1024;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  gemm_kernel<<<grid, kThreads, smem, s>>>(ma, mb, M, N, K, y, out_mode, status);
+  return cudaGetLastError();
+}
+
+}  // namespace akv

@@ -1,0 +1,135 @@
+"""Decoder layers of the single-prefill restoration: GEMM, RMSNorm, SwiGLU and
+the multi-layer forward with segmented attention, against fp64 references."""
+import numpy as np
+import pytest
+
+import kv_cache_drop_gb300 as akv
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+# Decoder outputs are final-RMSNorm states (unit RMS).  Every GEMM input is
+# rounded to bf16 (relative 2^-9) across four layers while the oracle runs
+# fp64 end to end: gate the relative RMS error at 2e-2 and the worst element
+# at 0.25 (about 8 sigma of that error at unit scale).
+MODEL_REL_RMS = 2e-2
+MODEL_MAX_ABS = 0.25
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _bf16(a, dev="cuda"):
+    return akv.to_device(np.ascontiguousarray(a), "bf16", dev)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 352, 200), (128, 256, 64), (1000, 1024, 1024),
+                                   (77, 4096, 1024)])
+def test_gemm_modes(M, N, K):
+    torch = _torch()
+    rng = np.random.default_rng(M + N + K)
+    x = workloads.gen._normals(rng, (M, K), "bf16")
+    w = workloads.gen._normals(rng, (N, K), "bf16", 0.05)
+    ref = oracle.widen(x, "bf16") @ oracle.widen(w, "bf16").T
+    scale = float(np.sqrt(np.mean(ref * ref)))
+    yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    akv.akv_gemm_bf16(M, N, K, _bf16(x), _bf16(w), yb, 0)
+    yf = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    akv.akv_gemm_bf16(M, N, K, _bf16(x), _bf16(w), yf, 1)
+    acc = torch.full((M, N), 0.5, dtype=torch.float32, device="cuda")
+    akv.akv_gemm_bf16(M, N, K, _bf16(x), _bf16(w), acc, 2)
+    torch.cuda.synchronize()
+    # fp32 accumulation over K products: relative error well under 1e-5 of scale
+    assert np.max(np.abs(yf.cpu().numpy() - ref)) <= 1e-4 * scale * np.sqrt(K / 64)
+    assert np.max(np.abs(acc.cpu().numpy() - 0.5 - ref)) <= 1e-4 * scale * np.sqrt(K / 64) + 1e-6
+    # bf16 store: one rounding, relative 2^-9
+    assert np.max(np.abs(yb.float().cpu().numpy() - ref) / (np.abs(ref) + 1e-3 * scale)) <= 2 ** -8
+
+
+def test_rmsnorm_and_swiglu():
+    torch = _torch()
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((37, 1024)).astype(np.float32) * 3
+    y = torch.empty((37, 1024), dtype=torch.float32, device="cuda")
+    akv.akv_rmsnorm(37, 1024, 1e-6, torch.from_numpy(x).cuda(), y)
+    ref = oracle.rmsnorm(x.astype(np.float64), 1e-6)
+    g = workloads.gen._normals(rng, (5000,), "bf16")
+    u = workloads.gen._normals(rng, (5000,), "bf16")
+    out = torch.empty(5000, dtype=torch.bfloat16, device="cuda")
+    akv.akv_swiglu(5000, _bf16(g), _bf16(u), out)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(y.cpu().numpy() - ref)) <= 1e-5
+    gg, uu = oracle.widen(g, "bf16"), oracle.widen(u, "bf16")
+    sref = gg / (1 + np.exp(-gg)) * uu
+    assert np.max(np.abs(out.float().cpu().numpy() - sref) / (np.abs(sref) + 1e-3)) <= 2 ** -7
+
+
+def _gpu_weights(mw):
+    return [{k: _bf16(np.ascontiguousarray(v.T)) for k, v in w.items()} for w in mw.weights]
+
+
+def run_decoder(mw, reqs=None):
+    """Forward of requests `reqs` (default all) of a model workload; returns
+    fp32 numpy [n_req * T, d]."""
+    torch = _torch()
+    reqs = list(range(mw.n_req)) if reqs is None else reqs
+    T = mw.T
+    shp = akv.shape(mw.Hq, mw.Hkv, mw.D, "bf16", mw.rope_base)
+    ops = [(mw.msg_start, *mw.ops[b]) for b in reqs]
+    cu = np.arange(len(reqs) + 1, dtype=np.int64) * T
+    plan = akv.Plan(shp, cu, ops)
+    x = _bf16(np.concatenate([mw.x] * len(reqs)))
+    out = torch.empty((len(reqs) * T, mw.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.empty(akv.akv_decoder_workspace(plan, mw.d_model, mw.d_ff), dtype=torch.uint8,
+                     device="cuda")
+    weights = _gpu_weights(mw)  # must outlive the asynchronous kernels
+    akv.akv_decoder_forward(plan, weights, mw.d_model, mw.d_ff, mw.eps, x, out, ws)
+    torch.cuda.synchronize()
+    del weights
+    assert akv.akv_workspace_status(ws) == 0, "a kernel barrier wait timed out"
+    return out.cpu().numpy()
+
+
+def _rel(got, ref):
+    d = got - ref
+    return float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(ref * ref))), float(np.abs(d).max())
+
+
+def test_decoder_small_vs_oracle():
+    """Three requests, 4 layers at the full layer shape (d 1024, 16/4 heads,
+    SwiGLU 4096), shared 128-token prefix + 640 diverging tokens."""
+    mw = workloads.model_workload(seed=5, n_req=3, prefix=128, following=640,
+                                  asst_len=(20, 60), tool_len=(60, 150))
+    got = run_decoder(mw)
+    T = mw.T
+    for b in range(mw.n_req):
+        ref = oracle.model_replay(mw.weights, mw.x, mw.msg_start, *mw.ops[b], mw.Hq, mw.Hkv,
+                                  mw.D, mw.rope_base, mw.eps)
+        rel, mx = _rel(got[b * T:(b + 1) * T], ref)
+        print(f"[parity] decoder request {b}: rel_rms={rel:.3e} max_abs={mx:.3e}")
+        assert rel <= MODEL_REL_RMS and mx <= MODEL_MAX_ABS
+
+
+def test_decoder_full_size_properties():
+    """32 requests x (8192 shared + 24576 diverging) tokens: every request's
+    shared-prefix rows are bit-identical, a request alone equals the same
+    request inside the batch bit for bit, and the first 1024 prefix rows
+    match the oracle."""
+    mw = workloads.model_workload()
+    T, P = mw.T, 8192
+    got = run_decoder(mw)
+    assert np.isfinite(got).all()
+    pref = got[:P]
+    for b in range(1, mw.n_req):
+        assert np.array_equal(got[b * T:b * T + P], pref), b
+    alone = run_decoder(mw, reqs=[5])
+    assert np.array_equal(alone, got[5 * T:6 * T])
+    n = 1024
+    ref = oracle.model_replay(mw.weights, mw.x[:n], np.array([0, n], np.int32), [], [], [],
+                              mw.Hq, mw.Hkv, mw.D, mw.rope_base, mw.eps)
+    rel, mx = _rel(pref[:n], ref)
+    print(f"[parity] decoder prefix rows: rel_rms={rel:.3e} max_abs={mx:.3e}")
+    assert rel <= MODEL_REL_RMS and mx <= MODEL_MAX_ABS
