@@ -324,6 +324,66 @@ def decode_part(dw, warmup_steps=8):
                 active_entries_per_step=n_total / dw.steps, launches_per_step=3)
 
 
+def decoder_part(mw, steps=3):
+    """The 4-layer decoder restoration (32 requests sharing a prefix): whole
+    forward, plus its segment attention and FFN GEMM timed alone."""
+    import torch
+    import kv_cache_drop_gb300 as akv
+    T1, n_req = mw.T, mw.n_req
+    T = T1 * n_req
+    shp = akv.shape(mw.Hq, mw.Hkv, mw.D, "bf16", mw.rope_base)
+    ops = [(mw.msg_start, *mw.ops[b]) for b in range(n_req)]
+    plan = akv.Plan(shp, np.arange(n_req + 1) * T1, ops)
+    weights = [{k: akv.to_device(np.ascontiguousarray(v.T), "bf16") for k, v in w.items()}
+               for w in mw.weights]
+    x = akv.to_device(np.concatenate([mw.x] * n_req), "bf16")
+    out = torch.empty((T, mw.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.empty(akv.akv_decoder_workspace(plan, mw.d_model, mw.d_ff), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    fwd_ms = timed(lambda: akv.akv_decoder_forward(plan, weights, mw.d_model, mw.d_ff, mw.eps, x,
+                                                   out, ws), steps)
+    status = akv.akv_workspace_status(ws)
+    del ws
+    vis = plan.info["visible_pairs"]
+    attn_flops = vis * 4 * mw.D * mw.Hq
+    dq, dkv = mw.Hq * mw.D, mw.Hkv * mw.D
+    gemm_flops = 2 * T * mw.d_model * (2 * dq + 2 * dkv + 3 * mw.d_ff)
+    q = torch.randn((T, mw.Hq, mw.D), device="cuda").to(torch.bfloat16)
+    k = torch.randn((T, mw.Hkv, mw.D), device="cuda").to(torch.bfloat16)
+    v = torch.randn((T, mw.Hkv, mw.D), device="cuda").to(torch.bfloat16)
+    o = torch.empty_like(q)
+    aws = plan.workspace()
+    akv.akv_segment_prepare(plan, q, k, v, aws)
+    attn_ms = timed(lambda: akv.akv_segment_attend(plan, o, aws), steps)
+    del q, k, v, o, aws
+    a = torch.randn((T, mw.d_model), device="cuda").to(torch.bfloat16)
+    g = torch.empty((T, mw.d_ff), dtype=torch.bfloat16, device="cuda")
+    gemm_ms = timed(lambda: akv.akv_gemm_bf16(T, mw.d_ff, mw.d_model, a, weights[0]["wg"], g, 0),
+                    steps)
+    del a, g, weights, x, out
+    torch.cuda.empty_cache()
+    return dict(requests=n_req, T=T, layers=mw.n_layers, visible_pairs_per_layer=int(vis),
+                forward_ms=fwd_ms,
+                forward_tflops=(mw.n_layers * (attn_flops + gemm_flops)) / fwd_ms / 1e9,
+                attn_ms=attn_ms, attn_tflops=attn_flops / attn_ms / 1e9,
+                ffn_gemm_ms=gemm_ms,
+                ffn_gemm_tflops=2 * T * mw.d_model * mw.d_ff / gemm_ms / 1e9,
+                status=status)
+
+
 def cpu_baseline(traj, seconds: float, seed: int = 0):
     """The oracle, as it stands, on a bounded sample of query rows."""
     import oracle
@@ -352,11 +412,13 @@ def run_ours(args, rank, world):
     import workloads
     akv.lib()
     pk = peaks()
-    if args.part in ("repos", "decode"):  # one secondary workload alone (profiling captures)
+    if args.part in ("repos", "decode", "decoder"):  # one secondary workload alone
         if args.part == "repos":
             res = repos_part(workloads.repos_config(), args.steps, args.warmup)
-        else:
+        elif args.part == "decode":
             res = decode_part(workloads.decode_workload())
+        else:
+            res = decoder_part(workloads.model_workload(), max(1, args.steps))
         return {"part": args.part, **res}
     traj = workloads.rolling_drop_config(rounds=args.rounds)
     main = prefill_part(traj, args.steps, args.warmup, world, with_e2e=not args.no_e2e)
@@ -388,6 +450,10 @@ def run_ours(args, rank, world):
         dp["frac_of_8tbs"] = dp["gbs"] / 8000.0
         parts["decode_14req_256steps"] = dp
         del dw
+        dec = decoder_part(workloads.model_workload())
+        dec["attn_frac_of_measured_sustained"] = dec["attn_tflops"] / pk["bf16_sus"]
+        dec["ffn_gemm_frac_of_measured_sustained"] = dec["ffn_gemm_tflops"] / pk["bf16_sus"]
+        parts["decoder_4layer_32req"] = dec
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup,
@@ -467,7 +533,7 @@ def main():
                     help="agent rounds of the headline trajectory (100 = the benchmark "
                          "workload; fewer only for small profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
-    ap.add_argument("--part", default="all", choices=["all", "repos", "decode"],
+    ap.add_argument("--part", default="all", choices=["all", "repos", "decode", "decoder"],
                     help="run one secondary workload alone (for profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":
