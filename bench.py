@@ -34,6 +34,22 @@ METRIC = "restore-prefill segment attn TFLOP/s (visible pairs); decode attn HBM 
 L2_BYTES = 129 * 2 ** 20
 
 
+def attn_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    record, or None when the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "attn_tc_kernel_rolling_drop_100r_dram.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    m = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            m.update(f.read())
+    return rec["traffic_bytes_per_launch"] if m.hexdigest() == rec["sources_sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -470,7 +486,8 @@ def run_ours(args, rank, world):
                            "tcgen05 segment attention"},
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                     "frac": round(attn_tflops / pk["bf16_sus"], 4), "traffic": None,
+                     "frac": round(attn_tflops / pk["bf16_sus"], 4),
+                     "traffic": attn_traffic() if args.rounds == 100 else None,
                      "kernel": "attn_tc_kernel",
                      "peak_note": f"{pk['src']} sustained bf16; of burst {pk['bf16']}: "
                                   f"{attn_tflops / pk['bf16']:.4f}"},
