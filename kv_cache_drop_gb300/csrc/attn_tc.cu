@@ -17,11 +17,14 @@
 // heads share every K/V window: GQA).  Warp roles:
 //   warps 0-3  softmax for head 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for head 1
-//   warp 8     TMA producer: Q tiles once, then K and V windows through a
-//              kStages-deep ring
+//   warp 8     TMA producer: K and V windows through a kStages-deep ring
 //   warp 9     TMEM allocator + single-thread tcgen05.mma issuer
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,336) O1 [336,416)
-// (O columns 64-79 hold the row sum).  P_i (fp16, two per 32-bit column)
+// (O columns 64-79 hold the row sum), Q0 [416,448) Q1 [448,480).  Q is
+// written into TMEM once per CTA by the softmax threads and is the A operand
+// of the score product, so that product reads only K from shared memory
+// (operands read from shared memory are limited to ~128 B/clk per SM, which
+// two shared-memory operands per MMA saturate).  P_i (fp16, two per 32-bit column)
 // overwrites the first 64 columns of S_i once S_i is in registers, and the
 // PV product reads it from there (A operand in TMEM): P never touches shared
 // memory, whose bandwidth the K=16 MMAs would otherwise saturate.  S_i(n+1)
@@ -51,7 +54,6 @@ constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units
 
 struct __align__(1024) Smem {
-  uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint8_t ones[kTileBytes];     // fp16 1.0, right after v: second MN atom of the PV B operand
@@ -81,7 +83,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, PlanDev p,
                    __nv_bfloat16 *__restrict__ out, int n_pairs) {
   extern __shared__ uint8_t smem_raw[];
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (int)p.T;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&sm.bar_q, 1);
+    ptx::mbar_init(&sm.bar_q, 256);  // both softmax groups wrote their Q into TMEM
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.bar_k[s], 1);
       ptx::mbar_init(&sm.bar_v[s], 1);
@@ -118,7 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kMmaWarp) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
   if (warp == kProdWarp && lane == 0) {
-    ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
   }
@@ -129,9 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     if (lane == 0) {
-      ptx::mbar_expect_tx(&sm.bar_q, 2 * kTileBytes);
-      ptx::tma_load_2d(sm.q[0], &tmQ, &sm.bar_q, 0, h0 * T + qt.t0);
-      ptx::tma_load_2d(sm.q[1], &tmQ, &sm.bar_q, 0, (h0 + 1) * T + qt.t0);
       const int krow = (qt.ver * p.Hkv + g) * T, vrow = g * T;
       for (int n = 0; n < n_win; ++n) {
         const int st = n % kStages;
@@ -157,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K-major operand, +128 per 16-key step of the MN-major V operand, and
       // 1024 per 16 KiB tile.
       constexpr uint64_t kTileStep = kTileBytes >> 4;
-      const uint64_t dq = desc_k_major(ptx::smem_addr(sm.q[0]));
       const uint64_t dk = desc_k_major(ptx::smem_addr(sm.k[0]));
       // V stage st: the ones atom is (kStages - st) tiles further on (LBO)
       uint64_t dv[kStages];
@@ -165,10 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < kStages; ++st)
         dv[st] = ptx::sdesc_sw128(ptx::smem_addr(sm.v[st]), (kStages - st) * kTileBytes);
       auto issue_s = [&](int i, int st) {
-        const uint64_t a0 = dq + i * kTileStep, b0 = dk + st * kTileStep;
+        const uint64_t b0 = dk + st * kTileStep;
+        // Q_i in TMEM: 64 dims as 32 packed columns, 8 per K step
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f16_ss(tmem + 128 * i, a0 + 2 * kk, b0 + 2 * kk, idS, kk > 0);
+          ptx::mma_f16_ts(tmem + 128 * i, tmem + 416 + 32 * i + 8 * kk, b0 + 2 * kk, idS, kk > 0);
         ptx::mma_commit(&sm.bar_s[i]);
       };
       auto issue_o = [&](int i, uint64_t vdesc, bool acc) {
@@ -218,6 +216,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + i * 128;
     const uint32_t tO = tmem + lane_base + 256 + i * 80;
     const uint32_t tL = tO + 64;  // row sums
+    {  // this row's rotated query (fp16, 64 dims = 32 packed words) into TMEM
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const __half *>(p.qr) +
+                                                          ((int64_t)(h0 + i) * T + t) * kD);
+      uint32_t qw[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * c] = x.x;
+        qw[4 * c + 1] = x.y;
+        qw[4 * c + 2] = x.z;
+        qw[4 * c + 3] = x.w;
+      }
+      ptx::tmem_st32(tmem + lane_base + 416 + 32 * i, qw);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.bar_q);
+    }
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
     int n_partial = 0;
@@ -387,9 +402,8 @@ bool make_map(CUtensorMap *m, void *base, int64_t rows, CUtensorMapDataType dt) 
 cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s) {
   if (p.n_qtiles == 0) return cudaSuccess;
   if ((p.Hq / p.Hkv) % 2) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.qr, (int64_t)p.Hq * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
-      !make_map(&mk, p.kr, (int64_t)p.max_ver * p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, p.kr, (int64_t)p.max_ver * p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
       !make_map(&mv, p.vp, (int64_t)p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return cudaErrorInvalidValue;
   const int smem = (int)sizeof(Smem) + 1024;
@@ -401,7 +415,7 @@ cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s) {
   }
   const int n_pairs = p.Hq / 2;
   const int64_t grid = (int64_t)p.n_qtiles * n_pairs;
-  attn_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p, (__nv_bfloat16 *)out,
+  attn_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(mk, mv, p, (__nv_bfloat16 *)out,
                                                         n_pairs);
   return cudaGetLastError();
 }
