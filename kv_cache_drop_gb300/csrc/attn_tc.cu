@@ -236,9 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
     int n_partial = 0;
+    // window list read two entries ahead, so no iteration waits on its load
     uint32_t win = p.windows[qt.win_off];
+    uint32_t win_nx = n_win > 1 ? p.windows[qt.win_off + 1] : 0u;
     for (int n = 0; n < n_win; ++n) {
-      const uint32_t win_next = n + 1 < n_win ? p.windows[qt.win_off + n + 1] : 0u;
+      const uint32_t win_next = win_nx;
+      win_nx = n + 2 < n_win ? p.windows[qt.win_off + n + 2] : 0u;
       const bool full = (win & kWinFull) != 0;
       // visibility bits of this row over the window's 128 keys
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
