@@ -285,13 +285,30 @@ def repos_part(traj, steps, warmup):
         if it >= warmup:
             t_cp.append(e[0].elapsed_time(e[1]))
     ms_cp = float(np.mean(t_cp))
+    # the same repos as one call: survivors found from per-message tables
+    # inside the kernel (includes the tables' upload on the stream)
+    bws = torch.empty(akv.akv_repos_boundary_workspace(traj.ops(), T), dtype=torch.uint8,
+                      device="cuda")
+    t_b = []
+    for it in range(warmup + steps):
+        flush_sum = flush.sum()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        akv.akv_repos_boundary(shp, traj.ops(), T, b, k, v, ko, vo, bws)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        if it >= warmup:
+            t_b.append(e[0].elapsed_time(e[1]))
+    ms_b = float(np.mean(t_b))
     del k, v, ko, vo, flush, src, dst
     torch.cuda.empty_cache()
     return dict(r=int(r), rotate_ms=ms_r, compact_ms=ms_c, bytes=int(bytes_rot),
                 rotate_gbs=bytes_rot / ms_r / 1e6,
                 same_size_copy_gbs=(4 * r * row) / ms_cp / 1e6,
                 frac_of_same_size_copy=(bytes_rot / ms_r) / ((4 * r * row) / ms_cp),
-                compact_plus_rotate_gbs=(bytes_rot + 8 * T) / (ms_r + ms_c) / 1e6)
+                compact_plus_rotate_gbs=(bytes_rot + 8 * T) / (ms_r + ms_c) / 1e6,
+                one_pass_ms=ms_b, one_pass_gbs=4 * r * row / ms_b / 1e6,
+                one_pass_frac_of_same_size_copy=ms_cp / ms_b)
 
 
 def repos_batch_part(dw, steps, warmup):

@@ -198,6 +198,22 @@ akv_status akv_repos_rotate(const akv_shape *shape, int32_t r, const int32_t *sr
                             const int32_t *pos_from, const int32_t *pos_to, const void *k_in,
                             const void *v_in, void *k_out, void *v_out, akv_stream_t stream);
 
+/* Repos at a boundary in one pass (section 3.3 drop + repos, Appendix
+ * A.1.2): the result of akv_compact at `upto` followed by akv_repos_rotate
+ * with src_idx = active_idx, pos_from = active_pos, pos_to = NULL, without
+ * the index lists.  k_in/v_in: device [T, Hkv, D] by logical index, keys
+ * rotated at their positions in the version current before a repos at
+ * `upto`.  k_out/v_out: device [>= n, Hkv, D], rows 0..n-1 written, K_out[j]
+ * rotated at position j; they must not overlap the inputs.  *n_out: host,
+ * the survivor count n (known when the call returns; 0 writes nothing).
+ * workspace: device, 256-byte aligned, akv_repos_boundary_workspace() bytes
+ * (three small per-message tables, uploaded on `stream`). */
+size_t akv_repos_boundary_workspace(const akv_oplog *ops, int32_t T);
+akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int32_t T,
+                              int32_t upto, const void *k_in, const void *v_in, void *k_out,
+                              void *v_out, int32_t *n_out, void *workspace,
+                              size_t workspace_bytes, akv_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Decode over the active cache (paper review page section 4 serving flow,
  * "decode reads only the active cache"; system README: drop/repos support

@@ -93,6 +93,11 @@ _SIGS = {
                                    ctypes.c_size_t, ctypes.c_void_p]),
     "akv_repos_rotate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
                          [ctypes.c_void_p] * 7 + [ctypes.c_void_p]),
+    "akv_repos_boundary_workspace": (ctypes.c_size_t, [ctypes.POINTER(OpLog), ctypes.c_int32]),
+    "akv_repos_boundary": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(OpLog),
+                                          ctypes.c_int32, ctypes.c_int32] +
+                           [ctypes.c_void_p] * 4 + [_i32p, ctypes.c_void_p, ctypes.c_size_t,
+                                                    ctypes.c_void_p]),
     "akv_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int32,
                                                ctypes.c_int32]),
     "akv_decode_attention": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
@@ -299,6 +304,23 @@ def akv_repos_rotate(shp: Shape, r: int, src_idx, pos_from, pos_to, k_in, v_in, 
     _check(lib().akv_repos_rotate(ctypes.byref(shp), r, _dev(src_idx), _dev(pos_from),
                                   _dev(pos_to), _dev(k_in), _dev(v_in), _dev(k_out), _dev(v_out),
                                   _stream(stream)))
+
+
+def akv_repos_boundary_workspace(ops, T: int) -> int:
+    o = _Ops([ops])
+    return lib().akv_repos_boundary_workspace(o.ptr(), T)
+
+
+def akv_repos_boundary(shp: Shape, ops, T: int, upto: int, k_in, v_in, k_out, v_out, workspace,
+                       stream=None) -> int:
+    """Survivors of boundary `upto` gathered, keys re-rotated to 0..n-1; returns n."""
+    o = _Ops([ops])
+    n = ctypes.c_int32(0)
+    _check(lib().akv_repos_boundary(ctypes.byref(shp), o.ptr(), T, upto, _dev(k_in), _dev(v_in),
+                                    _dev(k_out), _dev(v_out), ctypes.byref(n), _dev(workspace),
+                                    0 if workspace is None else workspace.numel(),
+                                    _stream(stream)))
+    return n.value
 
 
 def akv_decode_workspace(shp: Shape, B: int, max_kv: int) -> int:

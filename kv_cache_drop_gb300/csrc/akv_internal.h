@@ -79,6 +79,11 @@ cudaError_t launch_append(int dtype, int Hkv, int n, const void *kn, const void 
                           const int32_t *pos, const int32_t *slot, void *kp, void *vp,
                           const RopeTheta &th, cudaStream_t s);
 
+cudaError_t launch_repos_boundary(int dtype, int Hkv, int r, int nk, const int32_t *kstart,
+                                  const int32_t *kprefix, const int32_t *kpos, const void *kin,
+                                  const void *vin, void *kout, void *vout, const RopeTheta &th,
+                                  cudaStream_t s);
+
 struct CompactDev {
   const int32_t *msg_start;  // [n_msgs+1]
   const uint8_t *keep;       // [n_msgs] message survives the drops up to the boundary

@@ -672,6 +672,73 @@ akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *a
   return AKV_OK;
 }
 
+namespace {
+// Survivors after the drops of boundary `upto`, as runs of kept messages:
+// first row, first compacted index (exclusive prefix of kept lengths, with
+// the total appended), position of the first row in the version current
+// before any repos at `upto`.
+void kept_runs(const akv_oplog *o, const CompactHost &c, std::vector<int32_t> *kstart,
+               std::vector<int32_t> *kprefix, std::vector<int32_t> *kpos) {
+  int32_t j = 0, alive_base = 0;
+  for (int m = 0; m < c.n_msgs; ++m) {
+    const int32_t a = o->msg_start[m], len = o->msg_start[m + 1] - a;
+    int32_t pos0;
+    if (!c.has_br) pos0 = a;
+    else if (a < c.br_end) pos0 = alive_base;  // renumbered by the last earlier repos
+    else pos0 = c.r + (a - c.br_end);
+    if (c.has_br && a < c.br_end && c.alive_br[m]) alive_base += len;
+    if (!c.keep[m] || len == 0) continue;
+    kstart->push_back(a);
+    kprefix->push_back(j);
+    kpos->push_back(pos0);
+    j += len;
+  }
+  kprefix->push_back(j);
+}
+}  // namespace
+
+size_t akv_repos_boundary_workspace(const akv_oplog *ops, int32_t T) {
+  if (!ops || ops->n_msgs < 0) return 0;
+  (void)T;
+  return 3 * align_up(4 * (size_t)(ops->n_msgs + 1), 256);
+}
+
+akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int32_t T,
+                              int32_t upto, const void *k_in, const void *v_in, void *k_out,
+                              void *v_out, int32_t *n_out, void *workspace,
+                              size_t workspace_bytes, akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_repos_boundary")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (akv_status st = check_oplog(ops, T, 0)) return st;
+  if (!n_out) return fail(AKV_ERR_INVALID, "n_out is NULL");
+  CompactHost c;
+  if (akv_status st = compact_host(ops, upto, &c)) return st;
+  *n_out = (int32_t)c.n_active;
+  if (c.n_active == 0) return AKV_OK;
+  if (!k_in || !v_in || !k_out || !v_out) return fail(AKV_ERR_INVALID, "NULL tensor");
+  const size_t part = align_up(4 * (size_t)(ops->n_msgs + 1), 256), need = 3 * part;
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
+    return fail(AKV_ERR_WORKSPACE, "repos workspace: need %zu aligned bytes", need);
+  std::vector<int32_t> kstart, kprefix, kpos;
+  kept_runs(ops, c, &kstart, &kprefix, &kpos);
+  const int nk = (int)kstart.size();
+  cudaStream_t s = (cudaStream_t)stream;
+  char *b = (char *)workspace;
+  cudaError_t e = cudaMemcpyAsync(b, kstart.data(), 4 * nk, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + part, kprefix.data(), 4 * (nk + 1), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + 2 * part, kpos.data(), 4 * nk, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "repos tables upload");
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  e = launch_repos_boundary(shape->dtype, shape->Hkv, (int)c.n_active, nk, (const int32_t *)b,
+                            (const int32_t *)(b + part), (const int32_t *)(b + 2 * part), k_in,
+                            v_in, k_out, v_out, th, s);
+  if (e != cudaSuccess) return cuda_fail(e, "repos at boundary");
+  return AKV_OK;
+}
+
 // ------------------------------------------------------------------------
 // Repos rotate, append, decode
 // ------------------------------------------------------------------------

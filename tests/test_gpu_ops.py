@@ -83,6 +83,51 @@ def test_repos_compact_full_size():
     assert np.array_equal(vo.float().cpu().numpy(), rv)
 
 
+def _repos_boundary(r, upto, dtype, shp):
+    torch = _torch()
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    ko = torch.full((max(r.T, 1), shp.Hkv, 64), 7.0, dtype=tdt, device="cuda")
+    vo = torch.full_like(ko, 7.0)
+    ws = torch.empty(max(1, akv.akv_repos_boundary_workspace(r.ops(), r.T)), dtype=torch.uint8,
+                     device="cuda")
+    n = akv.akv_repos_boundary(shp, r.ops(), r.T, upto, akv.to_device(r.k, dtype),
+                               akv.to_device(r.v, dtype), ko, vo, ws)
+    torch.cuda.synchronize()
+    tail = ko[n:].float().cpu().numpy()
+    assert np.all(tail == 7.0) and np.all(vo[n:].float().cpu().numpy() == 7.0)  # rows >= n untouched
+    return ko[:n].float().cpu().numpy(), vo[:n].float().cpu().numpy()
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_repos_boundary_every_boundary(seed, dtype):
+    """One-pass repos at every boundary of random logs with several repos:
+    same survivors, positions and rotation as compaction then repos."""
+    r = workloads.random_request(90 + seed, n_msgs=12, max_len=2000 if seed < 2 else 60,
+                                 p_drop=0.3, p_repos=0.4, dtype=dtype)
+    shp = akv.shape(r.Hq, r.Hkv, 64, dtype)
+    tol = 2 ** -8 * 4 if dtype == "bf16" else 1e-5
+    for upto in list(range(r.n_msgs)) + [-1]:
+        gk, gv = _repos_boundary(r, upto, dtype, shp)
+        ou, op = oracle.compact(*r.ops(), upto=upto)
+        rk, rv = oracle.repos_rotate(r.k, r.v, ou, op, np.arange(len(ou)), dtype, 10000.0)
+        assert gk.shape == rk.shape
+        if len(ou):
+            assert np.max(np.abs(gk - rk)) <= tol
+            assert np.array_equal(gv, rv)
+
+
+def test_repos_boundary_full_size():
+    """128k trajectory, one-pass repos at its repos boundary."""
+    r = workloads.repos_config()
+    b = int(r.repos_after[0])
+    gk, gv = _repos_boundary(r, b, "bf16", akv.shape(64, 8, 64, "bf16"))
+    ou, op = oracle.compact(*r.ops(), upto=b)
+    rk, rv = oracle.repos_rotate(r.k, r.v, ou, op, np.arange(len(ou)), "bf16", 10000.0)
+    assert np.max(np.abs(gk - rk)) <= 2 ** -8 * 4
+    assert np.array_equal(gv, rv)
+
+
 def _decode_oracle(dw, step, q_step):
     """Oracle decode at `step`: active pool keys as stored, appended keys
     rotated by the oracle itself at their positions."""
