@@ -35,7 +35,8 @@
 // O stays in TMEM for the whole tile.  The running max is only raised (and O rescaled)
 // when it grows by more than 2^8, so O is rarely touched.
 // Every barrier wait is bounded; a timeout sets a bit in the workspace status
-// word, after which all waits in the grid return at once so the launch ends.
+// word, after which every blocked wait in the grid returns within a poll
+// interval (about 4 us) so the launch ends.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -44,7 +45,7 @@
 namespace akv {
 namespace {
 
-constexpr int kStages = 3;  // the V-descriptor selection below assumes 3
+constexpr int kStages = 5;
 constexpr int kThreads = 320;
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTileBytes = 128 * 64 * 2;  // 128 rows x 64 bf16
@@ -52,6 +53,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitBudget = 1000000000LL;  // SM clocks (~0.5 s)
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units
+// hardware named barriers (0 is __syncthreads)
+constexpr int kBarMask = 1;   // +i: softmax group i stages a window's key tags (128 threads)
+constexpr int kBarP = 3;      // +i: P_i in TMEM: group i arrives, the MMA warp syncs (160)
+constexpr int kBarKV = 5;     // +stage: K/V tile landed: producer arrives, MMA warp syncs (64)
+static_assert(kBarKV + kStages <= 16, "named barriers");
 
 struct __align__(1024) Smem {
   uint8_t k[kStages][kTileBytes];
@@ -59,24 +65,18 @@ struct __align__(1024) Smem {
   uint8_t ones[kTileBytes];     // fp16 1.0, right after v: second MN atom of the PV B operand
   int32_t mask_u[2][2][128];    // [head][buffer][column]
   int32_t mask_d[2][2][128];
-  uint64_t bar_q;
-  uint64_t bar_k[kStages], bar_v[kStages], bar_empty[kStages];
-  uint64_t bar_s[2], bar_p[2], bar_o[2], bar_done;
+  uint64_t bar_kv[kStages], bar_empty[kStages];
+  uint64_t bar_s[2], bar_o[2], bar_done;
   uint32_t tmem_base;
 };
 
-// Bounded wait; on timeout flags the grid (status word) so every later wait
-// returns immediately.  Control flow continues either way, so warp-collective
-// instructions stay convergent.
+// Bounded wait; on timeout flags the grid (status word) so that every wait
+// still blocked returns within a poll interval.  Control flow continues
+// either way, so warp-collective instructions stay convergent.
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_t *status) {
-  if (ptx::mbar_try_wait(bar, parity)) return;
-  if (*(volatile uint32_t *)status) return;
-  if (!ptx::mbar_wait(bar, parity, kWaitBudget)) atomicOr(status, kStatusWaitTimeout);
+  ptx::mbar_wait_grid(bar, parity, status, kStatusWaitTimeout, kWaitBudget);
 }
 
-__device__ __forceinline__ uint64_t desc_k_major(uint32_t saddr) {
-  return ptx::sdesc_sw128(saddr);
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -98,15 +98,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (int)p.T;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&sm.bar_q, 256);  // both softmax groups wrote their Q into TMEM
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&sm.bar_k[s], 1);
-      ptx::mbar_init(&sm.bar_v[s], 1);
+      ptx::mbar_init(&sm.bar_kv[s], 1);
       ptx::mbar_init(&sm.bar_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&sm.bar_s[i], 1);
-      ptx::mbar_init(&sm.bar_p[i], 128);
       ptx::mbar_init(&sm.bar_o[i], 1);
     }
     ptx::mbar_init(&sm.bar_done, 1);
@@ -129,82 +126,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == kProdWarp) {
-    if (lane == 0) {
-      const int krow = (qt.ver * p.Hkv + g) * T, vrow = g * T;
-      for (int n = 0; n < n_win; ++n) {
+    // The whole warp runs the loop (named barriers count all 32 lanes);
+    // lane 0 issues the copies.  Window n's tile is announced on named
+    // barrier kBarKV + stage once it has landed; the stage of window n-1 is
+    // refilled (with window n-1+kStages) once both heads' P.V(n-1) are done.
+    const int krow = (qt.ver * p.Hkv + g) * T, vrow = g * T;
+    auto load = [&](int n) {
+      if (lane == 0) {
         const int st = n % kStages;
-        if (n >= kStages) wait_bar(&sm.bar_empty[st], ((n / kStages) - 1) & 1, p.status);
         const int w = (int)(p.windows[qt.win_off + n] & ~kWinFull);
-        ptx::mbar_expect_tx(&sm.bar_k[st], kTileBytes);
-        ptx::tma_load_2d(sm.k[st], &tmK, &sm.bar_k[st], 0, krow + w);
-        ptx::mbar_expect_tx(&sm.bar_v[st], kTileBytes);
-        ptx::tma_load_2d(sm.v[st], &tmV, &sm.bar_v[st], 0, vrow + w);
+        ptx::mbar_expect_tx(&sm.bar_kv[st], 2 * kTileBytes);
+        ptx::tma_load_2d(sm.k[st], &tmK, &sm.bar_kv[st], 0, krow + w);
+        ptx::tma_load_2d(sm.v[st], &tmV, &sm.bar_kv[st], 0, vrow + w);
       }
-      // no copy may still be in flight when the CTA exits
-      for (int n = n_win > kStages ? n_win - kStages : 0; n < n_win; ++n) {
-        wait_bar(&sm.bar_k[n % kStages], (n / kStages) & 1, p.status);
-        wait_bar(&sm.bar_v[n % kStages], (n / kStages) & 1, p.status);
+    };
+    for (int n = 0; n < n_win && n < kStages; ++n) load(n);
+    for (int n = 0; n < n_win; ++n) {
+      wait_bar(&sm.bar_kv[n % kStages], (n / kStages) & 1, p.status);
+      ptx::named_bar_arrive(kBarKV + n % kStages, 64);
+      const int m = n - 1 + kStages;  // refill the stage of window n-1
+      if (n >= 1 && m < n_win) {
+        wait_bar(&sm.bar_empty[(n - 1) % kStages], ((n - 1) / kStages) & 1, p.status);
+        load(m);
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      constexpr uint32_t idS = ptx::idesc_f16(128, 128, false);  // fp16 Qr x fp16 Kr
-      constexpr uint32_t idO = ptx::idesc_f16(128, 80, true);    // fp16 P x [fp16 V | ones]
-      // Descriptors are built once; per MMA only a small constant is added to
-      // the address field (16-byte units): +2 per 16-element K step of a
-      // K-major operand, +128 per 16-key step of the MN-major V operand, and
-      // 1024 per 16 KiB tile.
-      constexpr uint64_t kTileStep = kTileBytes >> 4;
-      const uint64_t dk = desc_k_major(ptx::smem_addr(sm.k[0]));
-      // V stage st: the ones atom is (kStages - st) tiles further on (LBO)
-      uint64_t dv[kStages];
+    // The whole warp follows the loop (named barriers); lane 0 issues.  It
+    // never polls a shared-memory barrier between MMAs: each such poll costs
+    // the issuing thread ~200 clocks, during which the tensor core's short
+    // instruction queue runs dry.
+    constexpr uint32_t idS = ptx::idesc_f16(128, 128, false);  // fp16 Qr x fp16 Kr
+    constexpr uint32_t idO = ptx::idesc_f16(128, 80, true);    // fp16 P x [fp16 V | ones]
+    // Descriptors are built once; per MMA only a small constant is added to
+    // the address field (16-byte units): +2 per 16-element K step of a
+    // K-major operand, +128 per 16-key step of the MN-major V operand, and
+    // 1024 per 16 KiB tile.
+    constexpr uint64_t kTileStep = kTileBytes >> 4;
+    const uint64_t dk = ptx::sdesc_sw128(ptx::smem_addr(sm.k[0]));
+    // V stage st: start address one tile per stage further on, and the
+    // ones atom (kStages - st) tiles beyond it (leading-byte offset, bits 16-29)
+    const uint64_t dv0 = ptx::sdesc_sw128(ptx::smem_addr(sm.v[0]), kStages * kTileBytes);
+    const bool leader = lane == 0;
+    auto issue_s = [&](int i, int st) {
+      if (!leader) return;
+      const uint64_t b0 = dk + st * kTileStep;
+      // Q_i in TMEM: 64 dims as 32 packed columns, 8 per K step
 #pragma unroll
-      for (int st = 0; st < kStages; ++st)
-        dv[st] = ptx::sdesc_sw128(ptx::smem_addr(sm.v[st]), (kStages - st) * kTileBytes);
-      auto issue_s = [&](int i, int st) {
-        const uint64_t b0 = dk + st * kTileStep;
-        // Q_i in TMEM: 64 dims as 32 packed columns, 8 per K step
+      for (int kk = 0; kk < 4; ++kk)
+        ptx::mma_f16_ts(tmem + 128 * i, tmem + 416 + 32 * i + 8 * kk, b0 + 2 * kk, idS, kk > 0);
+      ptx::mma_commit(&sm.bar_s[i]);
+    };
+    auto issue_o = [&](int i, int st, bool acc) {
+      if (!leader) return;
+      const uint64_t vd = dv0 + (uint64_t)st * kTileStep - (((uint64_t)st * kTileStep) << 16);
+      // P_i: 128 keys as 64 packed columns at the start of S_i, 8 per K step
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f16_ts(tmem + 128 * i, tmem + 416 + 32 * i + 8 * kk, b0 + 2 * kk, idS, kk > 0);
-        ptx::mma_commit(&sm.bar_s[i]);
-      };
-      auto issue_o = [&](int i, uint64_t vdesc, bool acc) {
-        // P_i: 128 keys as 64 packed columns at the start of S_i, 8 per K step
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_f16_ts(tmem + 256 + 80 * i, tmem + 128 * i + 8 * kk, vdesc + 128 * kk, idO,
-                          (acc || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(&sm.bar_o[i]);
-      };
-      wait_bar(&sm.bar_q, 0, p.status);
-      wait_bar(&sm.bar_k[0], 0, p.status);
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_f16_ts(tmem + 256 + 80 * i, tmem + 128 * i + 8 * kk, vd + 128 * kk, idO,
+                        (acc || kk > 0) ? 1u : 0u);
+      ptx::mma_commit(&sm.bar_o[i]);
+    };
+    ptx::named_bar_sync(kBarP + 0, 160);  // Q_0 in TMEM
+    ptx::named_bar_sync(kBarP + 1, 160);  // Q_1 in TMEM
+    ptx::named_bar_sync(kBarKV + 0, 64);
+    ptx::tc_fence_after();
+    issue_s(0, 0);
+    issue_s(1, 0);
+    for (int n = 0; n < n_win; ++n) {
+      const int st = n % kStages;
+      const int st1 = (n + 1) % kStages;
+      ptx::named_bar_sync(kBarP + 0, 160);
       ptx::tc_fence_after();
-      issue_s(0, 0);
-      issue_s(1, 0);
-      for (int n = 0; n < n_win; ++n) {
-        const int st = n % kStages;
-        const int st1 = (n + 1) % kStages;
-        wait_bar(&sm.bar_v[st], (n / kStages) & 1, p.status);
-        static_assert(kStages == 3, "stage descriptor selection");
-        const uint64_t vdesc = st == 0 ? dv[0] : (st == 1 ? dv[1] : dv[2]);
-        wait_bar(&sm.bar_p[0], n & 1, p.status);
+      issue_o(0, st, n > 0);
+      if (n + 1 < n_win) {
+        ptx::named_bar_sync(kBarKV + st1, 64);
         ptx::tc_fence_after();
-        issue_o(0, vdesc, n > 0);
-        if (n + 1 < n_win) {
-          wait_bar(&sm.bar_k[st1], ((n + 1) / kStages) & 1, p.status);
-          ptx::tc_fence_after();
-          issue_s(0, st1);
-        }
-        wait_bar(&sm.bar_p[1], n & 1, p.status);
-        ptx::tc_fence_after();
-        issue_o(1, vdesc, n > 0);
-        if (n + 1 < n_win) issue_s(1, st1);
-        ptx::mma_commit(&sm.bar_empty[st]);
+        issue_s(0, st1);
       }
-      ptx::mma_commit(&sm.bar_done);
-      wait_bar(&sm.bar_done, 0, p.status);
+      ptx::named_bar_sync(kBarP + 1, 160);
+      ptx::tc_fence_after();
+      issue_o(1, st, n > 0);
+      if (n + 1 < n_win) issue_s(1, st1);
+      if (leader) ptx::mma_commit(&sm.bar_empty[st]);
     }
+    if (leader) ptx::mma_commit(&sm.bar_done);
+    wait_bar(&sm.bar_done, 0, p.status);
   } else {
     // softmax: i = head within the pair, row = query row = TMEM lane
     const int i = warp >> 2;
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st32(tmem + lane_base + 416 + 32 * i, qw);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.bar_q);
+      ptx::named_bar_arrive(kBarP + i, 160);
     }
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = (int)(win & ~kWinFull) + row;
         sm.mask_u[i][buf][row] = __ldg(p.slot_u + j);
         sm.mask_d[i][buf][row] = __ldg(p.slot_dseg + j);
-        ptx::named_bar_sync(1 + i, 128);
+        ptx::named_bar_sync(kBarMask + i, 128);
         const int32_t *mu = sm.mask_u[i][buf], *md = sm.mask_d[i][buf];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.bar_p[i]);
+      ptx::named_bar_arrive(kBarP + i, 160);  // P_i (and a rescaled O_i) are in TMEM
     }
     wait_bar(&sm.bar_o[i], (n_win - 1) & 1, p.status);
     ptx::tc_fence_after();

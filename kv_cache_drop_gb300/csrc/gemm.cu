@@ -29,9 +29,7 @@ struct __align__(1024) GemmSmem {
 };
 
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_t *status) {
-  if (ptx::mbar_try_wait(bar, parity)) return;
-  if (status && *(volatile uint32_t *)status) return;
-  if (!ptx::mbar_wait(bar, parity, kWaitBudget) && status) atomicOr(status, kStatusWaitTimeout);
+  ptx::mbar_wait_grid(bar, parity, status, kStatusWaitTimeout, kWaitBudget);
 }
 
 // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add into Y

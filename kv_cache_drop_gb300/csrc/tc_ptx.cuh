@@ -62,6 +62,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
   return true;
 }
 
+// Wait for a phase in a kernel whose waits share a grid-wide status word.
+// The word is read only once a wait has lasted `poll` clocks, and every
+// `poll` clocks after that: a global load on every wait would put its
+// latency (hundreds of clocks) on the pipeline's critical path.  Returns
+// early when `abort_bit` is set in the word (a wait elsewhere in the grid
+// gave up); after `budget` clocks sets `abort_bit` itself and returns false.
+__device__ __forceinline__ bool mbar_wait_grid(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                               uint32_t abort_bit, long long budget,
+                                               long long poll = 8192) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  long long next = poll;
+  while (!mbar_try_wait(bar, parity)) {
+    const long long dt = clock64() - t0;
+    if (dt >= next) {
+      if (status && (*(volatile uint32_t *)status & abort_bit)) return false;
+      if (dt > budget) {
+        if (status) atomicOr(status, abort_bit);
+        return false;
+      }
+      next = dt + poll;
+    }
+  }
+  return true;
+}
+
 // ---- TMA ----
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
@@ -87,6 +113,11 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Arrive on a named barrier without waiting (n counts every participating
+// thread, including those that wait on it with named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // ---- TMEM allocation (one full warp) ----
