@@ -27,8 +27,22 @@ struct QTile {
   int32_t win_cnt;  // number of 128-key windows
   int32_t seg_lo;   // segment of row t0 (request-relative)
   int32_t seg_hi;   // segment of the last row
+  int32_t pm_off;   // first visibility-mask block of the tile's partial windows
+  int32_t pm_cnt;   // number of partial (masked) windows
+  int32_t pad[2];
 };
-static_assert(sizeof(QTile) == 32, "QTile layout");
+static_assert(sizeof(QTile) == 48, "QTile layout");
+
+// A window that needs an in-tile mask: its rows' visibility bits are
+// precomputed once per plan (they do not depend on the head) into a block of
+// 128 rows x 128 bits, bit j of row r = key slot (slot0 + j) visible to row
+// (t0 + r).
+struct MaskWin {
+  int32_t t0;     // first row of the query tile (batch-global)
+  int32_t len;    // rows in the tile
+  int32_t slot0;  // first key slot of the window
+  int32_t pad;
+};
 
 // Device views of the plan tables and the rotated copies, all inside one
 // caller workspace.
@@ -42,6 +56,8 @@ struct PlanDev {
   const int32_t *slot_pos;   // [max_ver][T] position of the slot's key in each version
   const QTile *qtiles;       // [n_qtiles]
   const uint32_t *windows;   // [n_windows] slot start | kWinFull
+  const MaskWin *mwin;       // [n_mask] partial windows, in tile then window order
+  uint4 *mask;               // [n_mask][128 rows] visibility bits (words = keys 0-31, ..)
   const int32_t *order;      // [n_qtiles] tiles by decreasing window count
   void *qr;                  // [Hq][T][D]  rotated queries, head-major (fp16 for bf16 inputs)
   void *kr;                  // [max_ver][Hkv][T][D] rotated keys, permuted slots, head-major
@@ -50,6 +66,7 @@ struct PlanDev {
                              // (fp16 for bf16 inputs)
   int64_t T;
   int32_t n_qtiles;
+  int32_t n_mask;
   int32_t max_ver;
   int32_t Hq, Hkv;
   float rope_base;
@@ -72,6 +89,7 @@ cudaError_t launch_prep(const PlanDev &p, const void *q, const void *k, const vo
 cudaError_t launch_attn_simt_f32(const PlanDev &p, void *out, cudaStream_t s);
 cudaError_t launch_visible_counts(const PlanDev &p, int32_t *counts, cudaStream_t s);
 cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s);
+cudaError_t launch_masks(const PlanDev &p, cudaStream_t s);
 cudaError_t launch_repos(int dtype, int Hkv, int r, const int32_t *src, const int32_t *pf,
                          const int32_t *pt, const void *kin, const void *vin, void *kout,
                          void *vout, const RopeTheta &th, cudaStream_t s);

@@ -125,7 +125,7 @@ void akv::rope_theta(float base, RopeTheta *out) {
 // ------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t status, tok_qpos, tok_seg, slot_src, slot_u, slot_dseg, slot_pos, qtiles, windows,
+  size_t status, tok_qpos, tok_seg, slot_src, slot_u, slot_dseg, slot_pos, qtiles, windows, mwin, mask,
       order, qr, kr, vp, total;
 };
 
@@ -137,6 +137,7 @@ struct akv_plan {
   std::vector<int32_t> tok_pos, tok_seg, tok_ver, drop_seg;  // request-relative
   std::vector<int32_t> slot_src, slot_u, slot_dseg, slot_pos;
   std::vector<QTile> qtiles;
+  std::vector<MaskWin> mwin;
   std::vector<uint32_t> windows;
   std::vector<int32_t> order;
   int64_t visible_pairs = 0, n_full = 0, n_segments = 0;
@@ -247,6 +248,7 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
       q.ver = v;
       q.req = req;
       q.win_off = (int32_t)P->windows.size();
+      q.pm_off = (int32_t)P->mwin.size();
       q.seg_lo = tseg[t0];
       q.seg_hi = tseg[t1 - 1];
       // visible slot intervals, in slot order: groups with dseg > seg_lo, the
@@ -275,11 +277,13 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
           }
           P->windows.push_back((uint32_t)(c0 + a) | (full ? kWinFull : 0u));
           if (full) ++P->n_full;
+          else P->mwin.push_back({q.t0, q.len, (int32_t)(c0 + a), 0});
           cover_end = a + kTileK;
           a = cover_end;
         }
       }
       q.win_cnt = (int32_t)(P->windows.size() - q.win_off);
+      q.pm_cnt = (int32_t)(P->mwin.size() - q.pm_off);
       P->qtiles.push_back(q);
     }
   }
@@ -305,6 +309,8 @@ void layout_workspace(akv_plan *P) {
   w.slot_pos = take(4 * T * P->max_ver, 256);
   w.qtiles = take(sizeof(QTile) * nt, 256);
   w.windows = take(4 * nw, 256);
+  w.mwin = take(sizeof(MaskWin) * P->mwin.size(), 256);
+  w.mask = take((size_t)kTileQ * 16 * P->mwin.size(), 256);
   w.order = take(4 * nt, 256);
   w.qr = take(es * T * P->shape.Hq * kD, 1024);
   w.kr = take(es * T * P->shape.Hkv * kD * P->max_ver, 1024);
@@ -325,6 +331,9 @@ PlanDev device_view(const akv_plan *P, void *ws) {
   d.slot_pos = (const int32_t *)(b + w.slot_pos);
   d.qtiles = (const QTile *)(b + w.qtiles);
   d.windows = (const uint32_t *)(b + w.windows);
+  d.mwin = (const MaskWin *)(b + w.mwin);
+  d.mask = (uint4 *)(b + w.mask);
+  d.n_mask = (int32_t)P->mwin.size();
   d.order = (const int32_t *)(b + w.order);
   d.qr = b + w.qr;
   d.kr = b + w.kr;
@@ -355,6 +364,7 @@ akv_status upload_plan(const akv_plan *P, void *ws, cudaStream_t s) {
       {w.slot_pos, P->slot_pos.data(), 4 * P->slot_pos.size()},
       {w.qtiles, P->qtiles.data(), sizeof(QTile) * P->qtiles.size()},
       {w.windows, P->windows.data(), 4 * P->windows.size()},
+      {w.mwin, P->mwin.data(), sizeof(MaskWin) * P->mwin.size()},
       {w.order, P->order.data(), 4 * P->order.size()},
   };
   cudaError_t e = cudaMemsetAsync(b + w.status, 0, 256, s);
@@ -490,7 +500,9 @@ akv_status akv_segment_prepare(const akv_plan *P, const void *q, const void *k, 
   if (akv_status st = upload_plan(P, workspace, s)) return st;
   RopeTheta th;
   rope_theta(P->shape.rope_base, &th);
-  cudaError_t e = launch_prep(device_view(P, workspace), q, k, v, th, s);
+  const PlanDev d = device_view(P, workspace);
+  cudaError_t e = launch_prep(d, q, k, v, th, s);
+  if (e == cudaSuccess && P->shape.dtype == AKV_BF16) e = launch_masks(d, s);
   if (e != cudaSuccess) return cuda_fail(e, "rope/permute pre-pass");
   return AKV_OK;
 }

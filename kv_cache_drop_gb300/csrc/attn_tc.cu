@@ -54,7 +54,6 @@ constexpr long long kWaitBudget = 1000000000LL;  // SM clocks (~0.5 s)
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units
 // hardware named barriers (0 is __syncthreads)
-constexpr int kBarMask = 1;   // +i: softmax group i stages a window's key tags (128 threads)
 constexpr int kBarP = 3;      // +i: P_i in TMEM: group i arrives, the MMA warp syncs (160)
 constexpr int kBarKV = 5;     // +stage: K/V tile landed: producer arrives, MMA warp syncs (64)
 static_assert(kBarKV + kStages <= 16, "named barriers");
@@ -63,8 +62,6 @@ struct __align__(1024) Smem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint8_t ones[kTileBytes];     // fp16 1.0, right after v: second MN atom of the PV B operand
-  int32_t mask_u[2][2][128];    // [head][buffer][column]
-  int32_t mask_d[2][2][128];
   uint64_t bar_kv[kStages], bar_empty[kStages];
   uint64_t bar_s[2], bar_o[2], bar_done;
   uint32_t tmem_base;
@@ -217,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x & 127;
     const bool valid = row < qt.len;
     const int t = qt.t0 + row;
-    const int seg = p.tok_seg[valid ? t : qt.t0];
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + i * 128;
     const uint32_t tO = tmem + lane_base + 256 + i * 80;
@@ -241,7 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
+    // this row's visibility bits for the tile's partial windows (precomputed
+    // per plan), loaded one partial window ahead
     int n_partial = 0;
+    const uint4 *mrow = p.mask + (int64_t)qt.pm_off * kTileQ + row;
+    uint4 vis_next = qt.pm_cnt > 0 ? __ldg(mrow) : make_uint4(0u, 0u, 0u, 0u);
     // window list read two entries ahead, so no iteration waits on its load
     uint32_t win = p.windows[qt.win_off];
     uint32_t win_nx = n_win > 1 ? p.windows[qt.win_off + 1] : 0u;
@@ -251,22 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = (win & kWinFull) != 0;
       // visibility bits of this row over the window's 128 keys
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-      if (!full) {  // uniform over the group: stage the window's key tags
-        const int buf = n_partial & 1;
-        ++n_partial;
-        const int j = (int)(win & ~kWinFull) + row;
-        sm.mask_u[i][buf][row] = __ldg(p.slot_u + j);
-        sm.mask_d[i][buf][row] = __ldg(p.slot_dseg + j);
-        ptx::named_bar_sync(kBarMask + i, 128);
-        const int32_t *mu = sm.mask_u[i][buf], *md = sm.mask_d[i][buf];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t bits = 0;
-#pragma unroll 8
-          for (int c = 0; c < 32; ++c)
-            bits |= (uint32_t)(mu[32 * w + c] <= t && seg < md[32 * w + c]) << c;
-          vis[w] = bits;
-        }
+      if (!full) {
+        vis[0] = vis_next.x;
+        vis[1] = vis_next.y;
+        vis[2] = vis_next.z;
+        vis[3] = vis_next.w;
+        if (++n_partial < qt.pm_cnt) vis_next = __ldg(mrow + (int64_t)n_partial * kTileQ);
       }
       win = win_next;
       wait_bar(&sm.bar_s[i], n & 1, p.status);

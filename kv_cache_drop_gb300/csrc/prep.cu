@@ -118,6 +118,36 @@ cudaError_t prep(const PlanDev &p, const void *q, const void *k, const void *v,
 
 }  // namespace
 
+namespace {
+// Visibility bits of the windows that need an in-tile mask, once per plan
+// (heads share them): CTA = one window, thread = one query row.
+__global__ void __launch_bounds__(kTileQ) mask_kernel(PlanDev p) {
+  __shared__ int32_t su[kTileK], sd[kTileK];
+  const MaskWin mw = p.mwin[blockIdx.x];
+  const int r = threadIdx.x;
+  // slot tables are padded after T with never-visible entries
+  su[r] = p.slot_u[mw.slot0 + r];
+  sd[r] = p.slot_dseg[mw.slot0 + r];
+  __syncthreads();
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (r < mw.len) {
+    const int t = mw.t0 + r;
+    const int seg = p.tok_seg[t];
+#pragma unroll 8
+    for (int c = 0; c < kTileK; ++c)
+      w[c >> 5] |= (uint32_t)(su[c] <= t && seg < sd[c]) << (c & 31);
+  }
+  p.mask[(int64_t)blockIdx.x * kTileQ + r] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+}  // namespace
+
+cudaError_t launch_masks(const PlanDev &p, cudaStream_t s) {
+  if (p.n_mask == 0) return cudaSuccess;
+  static_assert(kTileQ == kTileK, "one thread per row and per key");
+  mask_kernel<<<(unsigned)p.n_mask, kTileQ, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PlanDev &p, const void *q, const void *k, const void *v,
                         const RopeTheta &th, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
