@@ -54,9 +54,12 @@ constexpr long long kWaitBudget = 1000000000LL;  // SM clocks (~0.5 s)
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
 constexpr float kRescaleThreshold = 8.0f;                 // log2 units
 // hardware named barriers (0 is __syncthreads)
-constexpr int kBarP = 3;      // +i: P_i in TMEM: group i arrives, the MMA warp syncs (160)
-constexpr int kBarKV = 5;     // +stage: K/V tile landed: producer arrives, MMA warp syncs (64)
-static_assert(kBarKV + kStages <= 16, "named barriers");
+// Named barrier kBarP + i, one generation per window n (plus one for the
+// prologue): softmax group i arrives once P_i(n) is in TMEM (128 threads),
+// the TMA producer syncs once window n+1 has landed (32), and the MMA warp
+// syncs before issuing P_i.V(n) and S_i(n+1) (32).
+constexpr int kBarP = 3;
+constexpr int kBarPCount = 192;
 
 struct __align__(1024) Smem {
   uint8_t k[kStages][kTileBytes];
@@ -124,9 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     // The whole warp runs the loop (named barriers count all 32 lanes);
-    // lane 0 issues the copies.  Window n's tile is announced on named
-    // barrier kBarKV + stage once it has landed; the stage of window n-1 is
-    // refilled (with window n-1+kStages) once both heads' P.V(n-1) are done.
+    // lane 0 issues the copies.  The producer takes part in every
+    // generation of both P barriers, so it cannot run ahead of them; it
+    // refills the stage of window n-1 while window n is in flight.
     const int krow = (qt.ver * p.Hkv + g) * T, vrow = g * T;
     auto load = [&](int n) {
       if (lane == 0) {
@@ -138,15 +141,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     for (int n = 0; n < n_win && n < kStages; ++n) load(n);
+    wait_bar(&sm.bar_kv[0], 0, p.status);
+    ptx::named_bar_sync(kBarP + 0, kBarPCount);
+    ptx::named_bar_sync(kBarP + 1, kBarPCount);
     for (int n = 0; n < n_win; ++n) {
-      wait_bar(&sm.bar_kv[n % kStages], (n / kStages) & 1, p.status);
-      ptx::named_bar_arrive(kBarKV + n % kStages, 64);
+      if (n + 1 < n_win)
+        wait_bar(&sm.bar_kv[(n + 1) % kStages], ((n + 1) / kStages) & 1, p.status);
+      ptx::named_bar_sync(kBarP + 0, kBarPCount);
+      ptx::named_bar_sync(kBarP + 1, kBarPCount);
       const int m = n - 1 + kStages;  // refill the stage of window n-1
       if (n >= 1 && m < n_win) {
         wait_bar(&sm.bar_empty[(n - 1) % kStages], ((n - 1) / kStages) & 1, p.status);
         load(m);
       }
     }
+    // every copy was waited for above: none is in flight when the CTA exits
   } else if (warp == kMmaWarp) {
     // The whole warp follows the loop (named barriers); lane 0 issues.  It
     // never polls a shared-memory barrier between MMAs: each such poll costs
@@ -183,24 +192,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (acc || kk > 0) ? 1u : 0u);
       ptx::mma_commit(&sm.bar_o[i]);
     };
-    ptx::named_bar_sync(kBarP + 0, 160);  // Q_0 in TMEM
-    ptx::named_bar_sync(kBarP + 1, 160);  // Q_1 in TMEM
-    ptx::named_bar_sync(kBarKV + 0, 64);
+    ptx::named_bar_sync(kBarP + 0, kBarPCount);  // Q_0 in TMEM, window 0 landed
+    ptx::named_bar_sync(kBarP + 1, kBarPCount);  // Q_1 in TMEM
     ptx::tc_fence_after();
     issue_s(0, 0);
     issue_s(1, 0);
     for (int n = 0; n < n_win; ++n) {
       const int st = n % kStages;
       const int st1 = (n + 1) % kStages;
-      ptx::named_bar_sync(kBarP + 0, 160);
+      ptx::named_bar_sync(kBarP + 0, kBarPCount);  // P_0(n) in TMEM, window n+1 landed
       ptx::tc_fence_after();
       issue_o(0, st, n > 0);
-      if (n + 1 < n_win) {
-        ptx::named_bar_sync(kBarKV + st1, 64);
-        ptx::tc_fence_after();
-        issue_s(0, st1);
-      }
-      ptx::named_bar_sync(kBarP + 1, 160);
+      if (n + 1 < n_win) issue_s(0, st1);
+      ptx::named_bar_sync(kBarP + 1, kBarPCount);
       ptx::tc_fence_after();
       issue_o(1, st, n > 0);
       if (n + 1 < n_win) issue_s(1, st1);
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st32(tmem + lane_base + 416 + 32 * i, qw);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::named_bar_arrive(kBarP + i, 160);
+      ptx::named_bar_arrive(kBarP + i, kBarPCount);
     }
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::named_bar_arrive(kBarP + i, 160);  // P_i (and a rescaled O_i) are in TMEM
+      ptx::named_bar_arrive(kBarP + i, kBarPCount);  // P_i (and a rescaled O_i) are in TMEM
     }
     wait_bar(&sm.bar_o[i], (n_win - 1) & 1, p.status);
     ptx::tc_fence_after();
