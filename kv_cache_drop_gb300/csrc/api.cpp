@@ -712,7 +712,7 @@ void kept_runs(const akv_oplog *o, const CompactHost &c, std::vector<int32_t> *k
 size_t akv_repos_boundary_workspace(const akv_oplog *ops, int32_t T) {
   if (!ops || ops->n_msgs < 0) return 0;
   (void)T;
-  return 3 * align_up(4 * (size_t)(ops->n_msgs + 1), 256);
+  return align_up(4 * (3 * (size_t)ops->n_msgs + 1), 256);
 }
 
 akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int32_t T,
@@ -728,25 +728,26 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
   *n_out = (int32_t)c.n_active;
   if (c.n_active == 0) return AKV_OK;
   if (!k_in || !v_in || !k_out || !v_out) return fail(AKV_ERR_INVALID, "NULL tensor");
-  const size_t part = align_up(4 * (size_t)(ops->n_msgs + 1), 256), need = 3 * part;
+  const size_t need = 4 * (3 * (size_t)ops->n_msgs + 1);
   if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
     return fail(AKV_ERR_WORKSPACE, "repos workspace: need %zu aligned bytes", need);
   std::vector<int32_t> kstart, kprefix, kpos;
   kept_runs(ops, c, &kstart, &kprefix, &kpos);
   const int nk = (int)kstart.size();
+  // one upload: [kstart | kprefix | kpos]
+  std::vector<int32_t> packed;
+  packed.reserve(3 * nk + 1);
+  packed.insert(packed.end(), kstart.begin(), kstart.end());
+  packed.insert(packed.end(), kprefix.begin(), kprefix.end());
+  packed.insert(packed.end(), kpos.begin(), kpos.end());
   cudaStream_t s = (cudaStream_t)stream;
-  char *b = (char *)workspace;
-  cudaError_t e = cudaMemcpyAsync(b, kstart.data(), 4 * nk, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(b + part, kprefix.data(), 4 * (nk + 1), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(b + 2 * part, kpos.data(), 4 * nk, cudaMemcpyHostToDevice, s);
+  int32_t *b = (int32_t *)workspace;
+  cudaError_t e = cudaMemcpyAsync(b, packed.data(), 4 * packed.size(), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "repos tables upload");
   RopeTheta th;
   rope_theta(shape->rope_base, &th);
-  e = launch_repos_boundary(shape->dtype, shape->Hkv, (int)c.n_active, nk, (const int32_t *)b,
-                            (const int32_t *)(b + part), (const int32_t *)(b + 2 * part), k_in,
-                            v_in, k_out, v_out, th, s);
+  e = launch_repos_boundary(shape->dtype, shape->Hkv, (int)c.n_active, nk, b, b + nk,
+                            b + 2 * nk + 1, k_in, v_in, k_out, v_out, th, s);
   if (e != cudaSuccess) return cuda_fail(e, "repos at boundary");
   return AKV_OK;
 }

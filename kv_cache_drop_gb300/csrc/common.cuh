@@ -28,20 +28,46 @@ __device__ __forceinline__ void rope_cs(double theta, double pos, float *c, floa
 // bits so that k * C1 and k * C2 are exact for |k| < 2^16 (Cody-Waite).  The
 // reduced angle is accurate to ~3e-7 rad.  Larger positions take the double
 // path above.
-__device__ __forceinline__ void rope_cs(const RopeTheta &th, int f, int pos, float *c, float *s) {
-  if (pos < -262144 || pos > 262144) {
-    rope_cs(th.th[f], (double)pos, c, s);
-    return;
-  }
+__device__ __forceinline__ void rope_cs_pair(float hi, float lo, int pos, float *c, float *s) {
   const float p = (float)pos;  // exact
-  const float ah = p * th.hi[f];
-  const float ae = fmaf(p, th.hi[f], -ah);  // exact error of the product
-  const float al = fmaf(p, th.lo[f], ae);
+  const float ah = p * hi;
+  const float ae = fmaf(p, hi, -ah);  // exact error of the product
+  const float al = fmaf(p, lo, ae);
   const float k = rintf(ah * 0.159154943091895336f);
   float r = fmaf(-k, 6.28125f, ah);            // 2*pi = 6.28125
   r = fmaf(-k, 1.93023681640625e-3f, r);       //      + 1.93023681640625e-3
   r = fmaf(-k, 5.0703633860393888e-6f, r);     //      + 5.07036338...e-6 (+ ~2e-13)
   sincosf(r + al, s, c);
+}
+__device__ __forceinline__ void rope_cs(const RopeTheta &th, int f, int pos, float *c, float *s) {
+  if (pos < -262144 || pos > 262144) {
+    rope_cs(th.th[f], (double)pos, c, s);
+    return;
+  }
+  rope_cs_pair(th.hi[f], th.lo[f], pos, c, s);
+}
+
+// The frequencies in shared memory.  A RopeTheta kernel parameter sits in
+// the constant bank, which serves loads whose index differs across the lanes
+// of a warp one address at a time; kernels that build cos/sin tables over
+// many (row, frequency) pairs copy the float pairs here once per CTA.
+struct ThetaSmem {
+  float hi[kD / 2], lo[kD / 2];
+};
+// Threads 0..D/2-1 copy; the caller synchronises before use.
+__device__ __forceinline__ void stage_theta(const RopeTheta &th, ThetaSmem &ts) {
+  if (threadIdx.x < kD / 2) {
+    ts.hi[threadIdx.x] = th.hi[threadIdx.x];
+    ts.lo[threadIdx.x] = th.lo[threadIdx.x];
+  }
+}
+__device__ __forceinline__ void rope_cs(const RopeTheta &th, const ThetaSmem &ts, int f, int pos,
+                                        float *c, float *s) {
+  if (pos < -262144 || pos > 262144) {
+    rope_cs(th.th[f], (double)pos, c, s);
+    return;
+  }
+  rope_cs_pair(ts.hi[f], ts.lo[f], pos, c, s);
 }
 
 // 16-byte chunks of one head row (D = 64): a bf16 chunk holds 8 elements, an

@@ -30,10 +30,13 @@ __global__ void __launch_bounds__(kThreads) prep_q_kernel(PlanDev p, const T *__
   constexpr int H = (kD / 2) / Chunk<T>::kElems;
   bool ovf = false;
   __shared__ float cs[kRows][kD / 2], sn[kRows][kD / 2];
+  __shared__ ThetaSmem ts;
+  stage_theta(th, ts);
+  __syncthreads();
   const int64_t t0 = (int64_t)blockIdx.x * kRows;
   for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
     const int r = i / (kD / 2), f = i % (kD / 2);
-    if (t0 + r < p.T) rope_cs(th, f, p.tok_qpos[t0 + r], &cs[r][f], &sn[r][f]);
+    if (t0 + r < p.T) rope_cs(th, ts, f, p.tok_qpos[t0 + r], &cs[r][f], &sn[r][f]);
   }
   __syncthreads();
   const int units = kRows * p.Hq * H;
@@ -59,12 +62,15 @@ __global__ void __launch_bounds__(kThreads) prep_kv_kernel(PlanDev p, const T *_
   __shared__ int32_t src[kRows];
   const int plane = blockIdx.y;  // < max_ver: key version; == max_ver: values
   const int64_t j0 = (int64_t)blockIdx.x * kRows;
+  __shared__ ThetaSmem ts;
   if (threadIdx.x < kRows && j0 + threadIdx.x < p.T) src[threadIdx.x] = p.slot_src[j0 + threadIdx.x];
   if (plane < p.max_ver) {
+    stage_theta(th, ts);
+    __syncthreads();
     for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
       const int r = i / (kD / 2), f = i % (kD / 2);
       if (j0 + r < p.T)
-        rope_cs(th, f, p.slot_pos[(int64_t)plane * p.T + j0 + r], &cs[r][f], &sn[r][f]);
+        rope_cs(th, ts, f, p.slot_pos[(int64_t)plane * p.T + j0 + r], &cs[r][f], &sn[r][f]);
     }
   }
   __syncthreads();
