@@ -222,7 +222,8 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
  * kv_indptr[b+1]) of k_pool/v_pool ([S, Hkv, D], keys stored already
  * rotated).  q_pos, kv_indptr ([B+1]), kv_indices: device int32.  max_kv:
  * host, an upper bound on any request's length (sizes the split-KV grid).
- * out [B, Hq, D] device.  A request with no keys gets zeros. */
+ * out [B, Hq, D] device.  A request with no keys gets zeros.
+ * Limit: B <= 65535 (AKV_ERR_UNSUPPORTED). */
 size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
 akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
                                 const int32_t *q_pos, const void *k_pool, const void *v_pool,

@@ -803,6 +803,7 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
   if (akv_status f = injected_fault("akv_decode_attention")) return f;
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
   if (B == 0) return AKV_OK;
   if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out || (max_kv > 0 && !kv_indices))
     return fail(AKV_ERR_INVALID, "NULL argument");
@@ -828,6 +829,7 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
   if (akv_status f = injected_fault("akv_decode_attention_static")) return f;
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
   if (B == 0) return AKV_OK;
   if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out || (max_kv > 0 && !kv_indices))
     return fail(AKV_ERR_INVALID, "NULL argument");

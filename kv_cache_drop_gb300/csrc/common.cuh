@@ -47,6 +47,25 @@ __device__ __forceinline__ void rope_cs(const RopeTheta &th, int f, int pos, flo
   rope_cs_pair(th.hi[f], th.lo[f], pos, c, s);
 }
 
+// cos/sin for a frequency index that differs across the lanes of a warp,
+// read from the RopeTheta kernel parameter with warp-uniform indices (an
+// unrolled select) instead of one divergent constant-bank load.
+__device__ __forceinline__ void rope_cs_lane(const RopeTheta &th, int f, int pos, float *c,
+                                             float *s) {
+  const bool wide = pos < -262144 || pos > 262144;
+  float hi = 0.f, lo = 0.f;
+  double t = 0.0;
+#pragma unroll
+  for (int i = 0; i < kD / 2; ++i)
+    if (i == f) {
+      hi = th.hi[i];
+      lo = th.lo[i];
+      if (wide) t = th.th[i];
+    }
+  if (wide) rope_cs(t, (double)pos, c, s);
+  else rope_cs_pair(hi, lo, pos, c, s);
+}
+
 // The frequencies in shared memory.  A RopeTheta kernel parameter sits in
 // the constant bank, which serves loads whose index differs across the lanes
 // of a warp one address at a time; kernels that build cos/sin tables over

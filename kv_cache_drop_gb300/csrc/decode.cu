@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int c0 = split * kChunk, c1 = min(n, c0 + kChunk);
   if (c0 >= n) return;  // the combine reads only the splits that hold keys
 
-  if (threadIdx.x < kD / 2) rope_cs(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
+  if (threadIdx.x < kD / 2) rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
   __syncthreads();
 
   // Q fragments (A operand, rows = query heads of the group, 16 rows padded
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(128)
   if (c0 >= n) return;
   if (threadIdx.x < kD / 2) {
     float c, s;
-    rope_cs(th, threadIdx.x, qpos[b], &c, &s);
+    rope_cs_lane(th, threadIdx.x, qpos[b], &c, &s);
     const float *qr = q + ((int64_t)b * Hq + h) * kD;
     const float x1 = qr[threadIdx.x], x2 = qr[threadIdx.x + kD / 2];
     qs[threadIdx.x] = (x1 * c - x2 * s) * 0.125f * kLog2e;
