@@ -391,11 +391,45 @@ def decode_part(dw, warmup_steps=8):
     n_total = sum(st["n"] for st in steps)
     bytes_total = n_total * (2 * row + 4) + dw.steps * dw.B * (2 * dw.Hq * 64 * 2 + 2 * row)
     ms = float(np.sum(per_step))
-    del kp, vp, ws, steps
+
+    # the same steps with rotation on read: the pool holds raw keys, every
+    # entry carries its position, the append is fused into the decode call
+    rng = np.random.default_rng(11)
+    pos_act = [np.sort(rng.choice(int(dw.L[b]), size=len(dw.active_slots[b]), replace=False))
+               for b in range(dw.B)]
+    for s in range(dw.steps):
+        kvpos = np.concatenate([np.concatenate([pos_act[b], dw.L[b] + np.arange(s + 1)])
+                                for b in range(dw.B)]).astype(np.int32)
+        steps[s]["kvpos"] = akv.i32_device(kvpos)
+
+    wsr = torch.empty(akv.akv_decode_rope_workspace(shp, dw.B, max_kv), dtype=torch.uint8,
+                      device="cuda")
+
+    def one_rope(st):
+        akv.akv_decode_attention_rope(shp, dw.B, st["q"], st["pos"], st["kn"], st["vn"],
+                                      st["slots"], kp, vp, st["indptr"], st["idx"], st["kvpos"],
+                                      max_kv, out, wsr)
+
+    for s in range(warmup_steps):
+        one_rope(steps[s])
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(dw.steps + 1)]
+    ev[0].record(stream)
+    for s in range(dw.steps):
+        one_rope(steps[s])
+        ev[s + 1].record(stream)
+    torch.cuda.synchronize()
+    ms_rope = float(np.sum([ev[s].elapsed_time(ev[s + 1]) for s in range(dw.steps)]))
+    bytes_rope = bytes_total + 4 * n_total  # + one position per entry
+    del kp, vp, ws, wsr, steps
     torch.cuda.empty_cache()
     return dict(B=dw.B, steps=dw.steps, ms_total=ms, ms_per_step=ms / dw.steps,
                 bytes_per_step=bytes_total / dw.steps, gbs=bytes_total / ms / 1e6,
-                active_entries_per_step=n_total / dw.steps, launches_per_step=3)
+                active_entries_per_step=n_total / dw.steps, launches_per_step=3,
+                rotate_on_read=dict(ms_per_step=ms_rope / dw.steps,
+                                    bytes_per_step=bytes_rope / dw.steps,
+                                    gbs=bytes_rope / ms_rope / 1e6, launches_per_step=2,
+                                    note="raw-key pool, per-entry positions, append fused"))
 
 
 def decoder_part(mw, steps=3):

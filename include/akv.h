@@ -231,6 +231,29 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
                                 int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
                                 akv_stream_t stream);
 
+/* Decode with rotation on read (the fused append and in-kernel repos of a
+ * serving step; paper review page section 3.3: a key moves between positions
+ * by a rotation, values are unchanged).  Same as akv_decode_attention except
+ * that k_pool holds keys BEFORE RoPE and kv_pos (device int32, parallel to
+ * kv_indices) gives each entry's current position: the kernel rotates each
+ * key by R(kv_pos[e]) as it reads it.  A repos then only rewrites kv_pos
+ * (e.g. 0..r-1) and the index order; no key is moved or re-rotated.
+ * Fused append (optional): k_new, v_new (device [B, Hkv, D], raw) and
+ * new_slot (device int32 [B]) are copied into pool slot new_slot[b] before
+ * that request's keys are read; request b's index list must then end with
+ * new_slot[b] (and its kv_pos entry with q_pos[b]).  Pass all three or none.
+ * k_pool/v_pool are written only at those slots.  Workspace: device,
+ * 256-byte aligned, akv_decode_rope_workspace() bytes (split-KV partials of
+ * 512-key chunks).  bf16 needs Hkv <= 8 or a multiple of 8. */
+size_t akv_decode_rope_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
+akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const void *q,
+                                     const int32_t *q_pos, const void *k_new, const void *v_new,
+                                     const int32_t *new_slot, void *k_pool, void *v_pool,
+                                     const int32_t *kv_indptr, const int32_t *kv_indices,
+                                     const int32_t *kv_pos, int32_t max_kv, void *out,
+                                     void *workspace, size_t workspace_bytes,
+                                     akv_stream_t stream);
+
 /* Decode without a workspace.  The paper has no counterpart: this entry
  * point exists for callers that cannot allocate device memory, so cannot
  * pass the workspace akv_decode_attention needs -- for example a plug-in

@@ -117,7 +117,12 @@ cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *ac
                            cudaStream_t s);
 int compact_blocks(int T);
 
-size_t decode_partials_bytes(int B, int Hq, int max_kv);
+size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope = false);
+cudaError_t launch_decode_rope(int dtype, int B, int Hq, int Hkv, const void *q,
+                               const int32_t *qpos, const void *k_new, const void *v_new,
+                               const int32_t *new_slot, void *kp, void *vp, const int32_t *indptr,
+                               const int32_t *indices, const int32_t *kvpos, int max_kv, void *out,
+                               void *ws, const RopeTheta &th, cudaStream_t s);
 cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, const int32_t *qpos,
                           const void *kp, const void *vp, const int32_t *indptr,
                           const int32_t *indices, int max_kv, void *out, void *ws,

@@ -821,6 +821,44 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
   return AKV_OK;
 }
 
+size_t akv_decode_rope_workspace(const akv_shape *shape, int32_t B, int32_t max_kv) {
+  if (!shape || B <= 0 || max_kv < 0) return 0;
+  return decode_partials_bytes(B, shape->Hq, max_kv, true);
+}
+
+akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const void *q,
+                                     const int32_t *q_pos, const void *k_new, const void *v_new,
+                                     const int32_t *new_slot, void *k_pool, void *v_pool,
+                                     const int32_t *kv_indptr, const int32_t *kv_indices,
+                                     const int32_t *kv_pos, int32_t max_kv, void *out,
+                                     void *workspace, size_t workspace_bytes,
+                                     akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_decode_attention_rope")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
+  if (B == 0) return AKV_OK;
+  if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out ||
+      (max_kv > 0 && (!kv_indices || !kv_pos)))
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  if ((new_slot == nullptr) != (k_new == nullptr) || (new_slot == nullptr) != (v_new == nullptr))
+    return fail(AKV_ERR_INVALID, "k_new, v_new and new_slot are given together or not at all");
+  if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
+  if (shape->dtype == AKV_BF16 && shape->Hkv > 8 && shape->Hkv % 8)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 rotate-on-read decode needs Hkv <= 8 or a multiple of 8");
+  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv, true);
+  if (need && (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need))
+    return fail(AKV_ERR_WORKSPACE, "decode (rotate on read) workspace: need %zu aligned bytes", need);
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_decode_rope(shape->dtype, B, shape->Hq, shape->Hkv, q, q_pos, k_new,
+                                     v_new, new_slot, k_pool, v_pool, kv_indptr, kv_indices,
+                                     kv_pos, max_kv, out, workspace, th, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode (rotate on read)");
+  return AKV_OK;
+}
+
 akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
                                        const int32_t *q_pos, const void *k_pool,
                                        const void *v_pool, const int32_t *kv_indptr,

@@ -23,6 +23,7 @@ namespace akv {
 namespace {
 
 constexpr int kChunk = 2048;  // keys per CTA
+constexpr int kRChunk = 512;  // keys per CTA of the rotate-on-read kernels (all heads of a block)
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;
 constexpr int kStages = 4;
@@ -33,10 +34,12 @@ struct Partials {
   float *o;   // [B][Hq][ns][kD]
 };
 
-__host__ __device__ inline int n_splits(int max_kv) { return max_kv <= 0 ? 1 : (max_kv + kChunk - 1) / kChunk; }
+__host__ __device__ inline int n_splits(int max_kv, int chunk = kChunk) {
+  return max_kv <= 0 ? 1 : (max_kv + chunk - 1) / chunk;
+}
 
-Partials partials(void *ws, int B, int Hq, int max_kv) {
-  const int ns = n_splits(max_kv);
+Partials partials(void *ws, int B, int Hq, int max_kv, int chunk = kChunk) {
+  const int ns = n_splits(max_kv, chunk);
   Partials p;
   p.ml = (float *)ws;
   const size_t ml_bytes = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
@@ -394,12 +397,385 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode with rotation on read.  The pool holds keys before RoPE and every
+// index entry carries its position, so a repos only rewrites the positions
+// (4 bytes per entry) instead of moving and re-rotating the keys.  The step's
+// append is fused: the CTA that owns a request's last key (the new token's
+// slot) first copies the new raw K/V rows into the pool.
+//
+// bf16: CTA = (key chunk, block of up to 8 KV heads, request), one warp per
+// KV head, all warps on the same 16-key tiles, so the warps together read
+// the keys' whole pool rows and share one cos/sin table per tile (16 keys x
+// 32 frequencies, built by all threads after the tile's positions land).
+// Each warp rotates its K fragments in registers (pairs d, d + 32 sit in
+// k-steps ks and ks + 2 of the same lane), splits them into bf16 hi + lo,
+// and runs the same tensor-core tile and online softmax as the kernel above.
+// ---------------------------------------------------------------------------
+constexpr int kRWarps = 8;   // KV heads per CTA
+constexpr int kRStages = 4;  // tiles in flight per warp
+constexpr int kRTileBytes = 4096 + 64;  // K tile, V tile, 16 positions
+constexpr int kRTabStride = kD / 2 + 2;  // float2 per key row: 4-way (minimal) bank spread
+constexpr int kRSmem = kRWarps * kRStages * kRTileBytes + 2 * kTileKeys * kRTabStride * 8;
+
+__global__ void __launch_bounds__(kRWarps * 32, 1)
+    decode_rope_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
+                            const int32_t *__restrict__ qpos, const __nv_bfloat16 *k_new,
+                            const __nv_bfloat16 *v_new, const int32_t *new_slot,
+                            __nv_bfloat16 *kp, __nv_bfloat16 *vp,
+                            const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                            const int32_t *__restrict__ kvpos, Partials part, RopeTheta th) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float qcs[kD / 2], qsn[kD / 2];
+  __shared__ ThetaSmem ts;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int ns = gridDim.x;
+  const int nw = blockDim.x >> 5;  // KV heads of this CTA
+  const int grp = Hq / Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = blockIdx.y * kRWarps + warp;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int beg = indptr[b], n = indptr[b + 1] - beg;
+  const int c0 = split * kRChunk, c1 = min(n, c0 + kRChunk);
+  if (c0 >= n) return;  // the combine reads only the splits that hold keys
+
+  stage_theta(th, ts);
+  if (new_slot && c1 == n) {  // fused append: this CTA owns the request's last key
+    const int64_t slot = new_slot[b];
+    for (int i = threadIdx.x; i < nw * 8; i += blockDim.x) {
+      const int gg = blockIdx.y * kRWarps + i / 8, c = i % 8;
+      const int64_t src = ((int64_t)b * Hkv + gg) * kD, dst = (slot * Hkv + gg) * kD;
+      reinterpret_cast<uint4 *>(kp + dst)[c] = reinterpret_cast<const uint4 *>(k_new + src)[c];
+      reinterpret_cast<uint4 *>(vp + dst)[c] = reinterpret_cast<const uint4 *>(v_new + src)[c];
+    }
+  }
+  __syncthreads();  // frequencies staged; appended rows visible to this CTA's gathers
+  if (threadIdx.x < kD / 2) rope_cs(th, ts, threadIdx.x, qpos[b], &qcs[threadIdx.x], &qsn[threadIdx.x]);
+  __syncthreads();
+
+  // query fragments of group g, rotated at the query position, split hi + lo
+  uint32_t qa[4][4], ql[4][4];
+  {
+    const float qs = 0.125f * kLog2e;
+    float qv[2][16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = gid + 8 * hh;
+      const bool ok = row < grp;
+      const __nv_bfloat16 *qrow = q + ((int64_t)b * Hq + g * grp + (ok ? row : 0)) * kD;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          qv[hh][ks * 4 + e] = ok ? __bfloat162float(qrow[d]) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          const float x1 = qv[hh][ks * 4 + e], x2 = qv[hh][(ks + 2) * 4 + e];
+          qv[hh][ks * 4 + e] = (x1 * qcs[d] - x2 * qsn[d]) * qs;
+          qv[hh][(ks + 2) * 4 + e] = (x1 * qsn[d] + x2 * qcs[d]) * qs;
+        }
+    auto lo = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
+      qa[ks][0] = pack_bf16(a0[0], a0[1]);
+      qa[ks][1] = pack_bf16(a1[0], a1[1]);
+      qa[ks][2] = pack_bf16(a0[2], a0[3]);
+      qa[ks][3] = pack_bf16(a1[2], a1[3]);
+      ql[ks][0] = pack_bf16(lo(a0[0]), lo(a0[1]));
+      ql[ks][1] = pack_bf16(lo(a1[0]), lo(a1[1]));
+      ql[ks][2] = pack_bf16(lo(a0[2]), lo(a0[3]));
+      ql[ks][3] = pack_bf16(lo(a1[2]), lo(a1[3]));
+    }
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  uint8_t *wsm = smem + warp * kRStages * kRTileBytes;
+  const uint32_t wsm_u = smem_u32(wsm);
+  // cos/sin table, double buffered: [buf][key][freq] as (cos, sin)
+  float2 *tab = reinterpret_cast<float2 *>(smem + kRWarps * kRStages * kRTileBytes);
+  const int n_tiles = (c1 - c0 + kTileKeys - 1) / kTileKeys;
+  auto issue = [&](int tile) {
+    const int stage = tile % kRStages;
+    if (tile < n_tiles) {
+      const int k0 = c0 + tile * kTileKeys;
+      int slot = 0;
+      const bool have = lane < kTileKeys && k0 + lane < c1;
+      if (have) slot = __ldg(indices + beg + k0 + lane);
+      if (lane < kTileKeys) {  // this tile's positions (0 past the end)
+        const uint32_t dst = wsm_u + stage * kRTileBytes + 4096 + 4 * lane;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst),
+                     "l"(kvpos + beg + (have ? k0 + lane : 0)), "r"(have ? 4 : 0));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = lane + 32 * i;  // 128 chunks per tile: key = idx/8, chunk = idx%8
+        const int key = idx >> 3, ch = idx & 7;
+        const int sl = __shfl_sync(0xffffffffu, slot, key);
+        const bool valid = k0 + key < c1;
+        const int64_t off = ((int64_t)sl * Hkv + g) * kD + ch * 8;
+        cp_async16(wsm_u + stage * kRTileBytes + swz(key, ch), kp + off, valid);
+        cp_async16(wsm_u + stage * kRTileBytes + 2048 + swz(key, ch), vp + off, valid);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
+  };
+
+#pragma unroll
+  for (int it = 0; it < kRStages - 1; ++it) issue(it);
+  for (int it = 0; it < n_tiles; ++it) {
+    issue(it + kRStages - 1);
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kRStages - 1));
+    __syncwarp();
+    const int stage = it % kRStages;
+    const uint32_t kt = wsm_u + stage * kRTileBytes, vt = kt + 2048;
+    const int32_t *tpos = reinterpret_cast<const int32_t *>(wsm + stage * kRTileBytes + 4096);
+    float2 *tb = tab + (it & 1) * kTileKeys * kRTabStride;
+    // this CTA's share of the tile's cos/sin table (every warp holds the
+    // same positions)
+    for (int e = threadIdx.x; e < kTileKeys * (kD / 2); e += blockDim.x) {
+      const int key = e / (kD / 2), f = e % (kD / 2);
+      float c, sn;
+      rope_cs(th, ts, f, tpos[key], &c, &sn);
+      tb[key * kRTabStride + f] = make_float2(c, sn);
+    }
+    __syncthreads();
+    const int k0 = c0 + it * kTileKeys;
+    // K fragments of the tile, rotated in registers: lane holds keys gid and
+    // gid + 8, dims 16ks + 2tig + {0, 1} (+8); d < 32 pairs with d + 32
+    uint32_t kb[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int mi = lane >> 3;
+      const int key = (mi >> 1) * 8 + (lane & 7);
+      const int ch = ks * 2 + (mi & 1);
+      ldsm_x4(kt + swz(key, ch), kb[ks][0], kb[ks][1], kb[ks][2], kb[ks][3]);
+    }
+    // The rotated key is split like the query, hi = bf16(k), lo = bf16(k - hi),
+    // and S = qhi khi + qlo khi + qhi klo: the scores see the rotated key to
+    // ~16 bits, as if it were exact, at a third more (idle) MMA work.
+    uint32_t kl[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
+        const int key = gid + 8 * (r >> 1);
+        const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
+        const float4 cs2 = *reinterpret_cast<const float4 *>(tb + key * kRTabStride + f);  // f, f+1
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
+        __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
+        const float x1a = __low2float(a), x1b = __high2float(a);
+        const float x2a = __low2float(bq), x2b = __high2float(bq);
+        const float y1a = x1a * cs2.x - x2a * cs2.y, y1b = x1b * cs2.z - x2b * cs2.w;
+        const float y2a = x1a * cs2.y + x2a * cs2.x, y2b = x1b * cs2.w + x2b * cs2.z;
+        kb[ks][r] = pack_bf16(y1a, y1b);
+        kb[ks + 2][r] = pack_bf16(y2a, y2b);
+        const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
+        const __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
+        kl[ks][r] = pack_bf16(y1a - __low2float(h1), y1b - __high2float(h1));
+        kl[ks + 2][r] = pack_bf16(y2a - __low2float(h2), y2b - __high2float(h2));
+      }
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      mma_bf16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+      mma_bf16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+      mma_bf16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+      mma_bf16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+      mma_bf16(s[0], qa[ks], kl[ks][0], kl[ks][1]);
+      mma_bf16(s[1], qa[ks], kl[ks][2], kl[ks][3]);
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = k0 + nb * 8 + 2 * tig + (e & 1);
+        if (key >= c1) s[nb][e] = -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+      }
+    float alpha[2], mref[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mn = fmaxf(m[r], mx[r]);
+      mref[r] = mn == -INFINITY ? 0.f : mn;
+      alpha[r] = exp2f(m[r] - mref[r]);
+      m[r] = mn;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nb][e] = exp2f(s[nb][e] - mref[e >> 1]);
+        rs[e >> 1] += s[nb][e];
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + rs[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int nb2 = 0; nb2 < 4; ++nb2) {
+      const int mi = lane >> 3;
+      const int key = (mi & 1) * 8 + (lane & 7);
+      const int ch = nb2 * 2 + (mi >> 1);
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vt + swz(key, ch), v0, v1, v2, v3);
+      mma_bf16(o[2 * nb2], pa, v0, v1);
+      mma_bf16(o[2 * nb2 + 1], pa, v2, v3);
+    }
+    __syncwarp();
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::);
+
+  // one warp per KV head: its rows are final partials
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int row = gid + 8 * hh;
+    if (row >= grp) continue;
+    const int64_t pi = ((int64_t)b * Hq + g * grp + row) * ns + split;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<float2 *>(part.o + pi * kD + i * 8 + 2 * tig) =
+          make_float2(o[i][2 * hh], o[i][2 * hh + 1]);
+    if (tig == 0) {
+      part.ml[2 * pi] = m[hh];
+      part.ml[2 * pi + 1] = l[hh];
+    }
+  }
+}
+
+// fp32 with rotation on read: thread per key, block of 128 threads per
+// (split, query head, request).  The new rows are appended by every CTA of
+// the last split before it reads (identical values).
+__global__ void __launch_bounds__(128)
+    decode_rope_f32_kernel(int Hq, int Hkv, const float *__restrict__ q,
+                           const int32_t *__restrict__ qpos, const float *k_new,
+                           const float *v_new, const int32_t *new_slot, float *kp, float *vp,
+                           const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                           const int32_t *__restrict__ kvpos, Partials part, RopeTheta th) {
+  __shared__ float qs[kD];
+  __shared__ float red_m[4], red_l[4];
+  __shared__ float red_o[4][kD];
+  __shared__ ThetaSmem ts;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int ns = gridDim.x, g = h / (Hq / Hkv);
+  const int beg = indptr[b], n = indptr[b + 1] - beg;
+  const int c0 = split * kRChunk, c1 = min(n, c0 + kRChunk);
+  if (c0 >= n) return;
+  stage_theta(th, ts);
+  if (new_slot && c1 == n && threadIdx.x < kD) {
+    const int64_t slot = new_slot[b];
+    kp[(slot * Hkv + g) * kD + threadIdx.x] = k_new[((int64_t)b * Hkv + g) * kD + threadIdx.x];
+    vp[(slot * Hkv + g) * kD + threadIdx.x] = v_new[((int64_t)b * Hkv + g) * kD + threadIdx.x];
+  }
+  __syncthreads();
+  if (threadIdx.x < kD / 2) {
+    float c, s;
+    rope_cs(th, ts, threadIdx.x, qpos[b], &c, &s);
+    const float *qr = q + ((int64_t)b * Hq + h) * kD;
+    const float x1 = qr[threadIdx.x], x2 = qr[threadIdx.x + kD / 2];
+    qs[threadIdx.x] = (x1 * c - x2 * s) * 0.125f * kLog2e;
+    qs[threadIdx.x + kD / 2] = (x1 * s + x2 * c) * 0.125f * kLog2e;
+  }
+  __syncthreads();
+  float m = -INFINITY, l = 0.f, acc[kD];
+#pragma unroll
+  for (int d = 0; d < kD; ++d) acc[d] = 0.f;
+  for (int k = c0 + threadIdx.x; k < c1; k += 128) {
+    const int64_t row = ((int64_t)indices[beg + k] * Hkv + g) * kD;
+    const int pos = kvpos[beg + k];
+    float sc = 0.f;
+#pragma unroll 4
+    for (int f = 0; f < kD / 2; ++f) {
+      float c, sn;
+      rope_cs(th, ts, f, pos, &c, &sn);
+      const float x1 = kp[row + f], x2 = kp[row + f + kD / 2];
+      sc = fmaf(qs[f], x1 * c - x2 * sn, sc);
+      sc = fmaf(qs[f + kD / 2], x1 * sn + x2 * c, sc);
+    }
+    const float mn = fmaxf(m, sc);
+    const float a = exp2f(m - mn), e = exp2f(sc - mn);
+    l = l * a + e;
+#pragma unroll
+    for (int d = 0; d < kD; ++d) acc[d] = fmaf(acc[d], a, e * vp[row + d]);
+    m = mn;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float M = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+  float L = l * f;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+#pragma unroll
+  for (int d = 0; d < kD; ++d) {
+    float x = acc[d] * f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) red_o[warp][d] = x;
+  }
+  if (lane == 0) {
+    red_m[warp] = M;
+    red_l[warp] = L;
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    float MM = -INFINITY;
+    for (int w = 0; w < 4; ++w) MM = fmaxf(MM, red_m[w]);
+    const float Mr = MM == -INFINITY ? 0.f : MM;
+    float LL = 0.f, x = 0.f;
+    for (int w = 0; w < 4; ++w) {
+      const float ff = exp2f(red_m[w] - Mr);
+      LL += red_l[w] * ff;
+      x += red_o[w][threadIdx.x] * ff;
+    }
+    const int64_t pi = ((int64_t)b * Hq + h) * ns + split;
+    part.o[pi * kD + threadIdx.x] = x;
+    if (threadIdx.x == 0) {
+      part.ml[2 * pi] = MM;
+      part.ml[2 * pi + 1] = LL;
+    }
+  }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kD) decode_combine_kernel(int Hq, int ns, const int32_t *indptr,
-                                                            Partials part, T *out) {
+__global__ void __launch_bounds__(kD) decode_combine_kernel(int Hq, int ns, int chunk,
+                                                            const int32_t *indptr, Partials part,
+                                                            T *out) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const int n = indptr[b + 1] - indptr[b];
-  const int used = n <= 0 ? 0 : min(ns, (n + kChunk - 1) / kChunk);
+  const int used = n <= 0 ? 0 : min(ns, (n + chunk - 1) / chunk);
   const int64_t base = ((int64_t)b * Hq + h) * ns;
   float M = -INFINITY;
   for (int s = 0; s < used; ++s) M = fmaxf(M, part.ml[2 * (base + s)]);
@@ -418,8 +794,8 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(int Hq, int ns, cons
 
 }  // namespace
 
-size_t decode_partials_bytes(int B, int Hq, int max_kv) {
-  const int ns = n_splits(max_kv);
+size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope) {
+  const int ns = n_splits(max_kv, rope ? kRChunk : kChunk);
   const size_t ml = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
   const size_t o = ((size_t)B * Hq * ns * kD * 4 + 255) / 256 * 256;
   return ml + o;
@@ -444,13 +820,46 @@ cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, cons
     decode_bf16_kernel<<<grid, kWarps * 32, smem, s>>>(
         Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
         (const __nv_bfloat16 *)vp, indptr, indices, part, th);
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part,
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part,
                                                                     (__nv_bfloat16 *)out);
   } else {
     dim3 grid(ns, Hq, B);
     decode_f32_kernel<<<grid, 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos, (const float *)kp,
                                           (const float *)vp, indptr, indices, part, th);
-    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part, (float *)out);
+    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part, (float *)out);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_rope(int dtype, int B, int Hq, int Hkv, const void *q,
+                               const int32_t *qpos, const void *k_new, const void *v_new,
+                               const int32_t *new_slot, void *kp, void *vp, const int32_t *indptr,
+                               const int32_t *indices, const int32_t *kvpos, int max_kv, void *out,
+                               void *ws, const RopeTheta &th, cudaStream_t s) {
+  const int ns = n_splits(max_kv, kRChunk);
+  Partials part = partials(ws, B, Hq, max_kv, kRChunk);
+  if (dtype == AKV_BF16) {
+    static bool attr = false;  // once per process (single device use)
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(decode_rope_bf16_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    const int hb = (Hkv + kRWarps - 1) / kRWarps;
+    // every head block has min(Hkv, 8) warps; Hkv is a multiple of 8 or below 8
+    const int nw = Hkv < kRWarps ? Hkv : kRWarps;
+    decode_rope_bf16_kernel<<<dim3(ns, hb, B), nw * 32, kRSmem, s>>>(
+        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)k_new,
+        (const __nv_bfloat16 *)v_new, new_slot, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
+        indices, kvpos, part, th);
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kRChunk, indptr, part,
+                                                                    (__nv_bfloat16 *)out);
+  } else {
+    decode_rope_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(
+        Hq, Hkv, (const float *)q, qpos, (const float *)k_new, (const float *)v_new, new_slot,
+        (float *)kp, (float *)vp, indptr, indices, kvpos, part, th);
+    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kRChunk, indptr, part, (float *)out);
   }
   return cudaGetLastError();
 }
@@ -502,13 +911,13 @@ cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *
     decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
         Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
         (const __nv_bfloat16 *)vp, indptr, indices, part, th);
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part,
+    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part,
                                                                     (__nv_bfloat16 *)out);
   } else {
     decode_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos,
                                                       (const float *)kp, (const float *)vp,
                                                       indptr, indices, part, th);
-    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, indptr, part, (float *)out);
+    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part, (float *)out);
   }
   return cudaGetLastError();
 }

@@ -209,6 +209,117 @@ def test_decode_full_size_steps():
         assert_close(got, _decode_oracle(dw, step, oracle.widen(dw.q[step], "bf16")), "bf16")
 
 
+def _rope_positions(dw, seed=11):
+    """Positions of the active entries when the pool holds raw keys: request
+    b's survivors sit at a sorted random subset of 0..L_b-1."""
+    rng = np.random.default_rng(seed)
+    return [np.sort(rng.choice(int(dw.L[b]), size=len(dw.active_slots[b]), replace=False))
+            .astype(np.int32) for b in range(dw.B)]
+
+
+def _decode_rope_oracle(dw, step, pos_act, q_step, renumber=False):
+    """fp64 decode at `step` over raw keys rotated at their positions; with
+    `renumber` every entry of request b is at its list index (a repos) and the
+    query follows them."""
+    out = []
+    for b in range(dw.B):
+        ka = oracle.widen(dw.k_pool[dw.active_slots[b]], dw.dtype)
+        kn = oracle.widen(dw.k_new[:step + 1, b], dw.dtype)
+        K = np.concatenate([ka, kn])
+        V = np.concatenate([oracle.widen(dw.v_pool[dw.active_slots[b]], dw.dtype),
+                            oracle.widen(dw.v_new[:step + 1, b], dw.dtype)])
+        if renumber:
+            pos = np.arange(len(K))
+        else:
+            pos = np.concatenate([pos_act[b], dw.L[b] + np.arange(step + 1)])
+        Kr = oracle.rope(K, pos[:, None], dw.rope_base)
+        o = oracle.decode_attention(q_step[b:b + 1], np.array([pos[-1]]), Kr, V,
+                                    np.array([0, len(K)]), np.arange(len(K)), "f64", dw.rope_base)
+        out.append(o[0])
+    return np.stack(out)
+
+
+def _run_decode_rope(dw, check_steps, pos_act, renumber_from=None):
+    """Rotate-on-read decode with the append fused; from step `renumber_from`
+    on, every request's entries are renumbered 0..n-1 (a repos done by
+    rewriting positions only)."""
+    torch = _torch()
+    shp = akv.shape(dw.Hq, dw.Hkv, 64, dw.dtype)
+    kp = akv.to_device(dw.k_pool, dw.dtype)
+    vp = akv.to_device(dw.v_pool, dw.dtype)
+    max_kv = max(len(a) for a in dw.active_slots) + dw.steps
+    ws = torch.empty(max(1, akv.akv_decode_rope_workspace(shp, dw.B, max_kv)), dtype=torch.uint8,
+                     device="cuda")
+    results = {}
+    for step in range(dw.steps):
+        indptr, idx = dw.indices_at(step)
+        ren = renumber_from is not None and step >= renumber_from
+        kvpos, qpos = [], []
+        for b in range(dw.B):
+            n = int(indptr[b + 1] - indptr[b])
+            p = (np.arange(n) if ren else
+                 np.concatenate([pos_act[b], dw.L[b] + np.arange(step + 1)]))
+            kvpos.append(p)
+            qpos.append(p[-1])
+        q = akv.to_device(dw.q[step], dw.dtype)
+        out = torch.empty_like(q)
+        akv.akv_decode_attention_rope(
+            shp, dw.B, q, akv.i32_device(np.array(qpos)), akv.to_device(dw.k_new[step], dw.dtype),
+            akv.to_device(dw.v_new[step], dw.dtype), akv.i32_device(dw.append_slots[step]), kp, vp,
+            akv.i32_device(indptr), akv.i32_device(idx), akv.i32_device(np.concatenate(kvpos)),
+            max_kv, out, ws)
+        if step in check_steps:
+            torch.cuda.synchronize()
+            results[step] = out.float().cpu().numpy()
+    torch.cuda.synchronize()
+    return results, kp, vp
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_rope_small(dtype):
+    """Raw-key pool, positions per entry, append fused: three steps against
+    fp64, and the appended raw rows land in the pool."""
+    dw = workloads.decode_workload(seed=8, B=3, active=(100, 5000), steps=3, Hq=8, Hkv=2,
+                                   dtype=dtype)
+    pos = _rope_positions(dw)
+    res, kp, vp = _run_decode_rope(dw, {0, 1, 2}, pos)
+    for step, got in res.items():
+        assert_close(got, _decode_rope_oracle(dw, step, pos, oracle.widen(dw.q[step], dtype)),
+                     dtype)
+    torch = _torch()
+    sl = torch.from_numpy(dw.append_slots.reshape(-1).astype(np.int64)).cuda()
+    for pool, new in ((kp, dw.k_new), (vp, dw.v_new)):
+        got = pool[sl]
+        got = got.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else \
+            got.cpu().numpy()
+        assert np.array_equal(got, new.reshape(-1, dw.Hkv, 64))  # raw rows, bit for bit
+
+
+def test_decode_rope_repos_by_positions():
+    """A repos mid-decode done by rewriting positions only (entries renumbered
+    0..n-1, keys untouched): matches fp64 with the keys rotated at the new
+    positions, before and after."""
+    dw = workloads.decode_workload(seed=12, B=4, active=(500, 6000), steps=4, Hq=16, Hkv=4)
+    dw.q[3] = workloads.bf16_bits(oracle.widen(dw.q[3], "bf16").astype(np.float32) * 8)  # peaky
+    pos = _rope_positions(dw, seed=13)
+    res, _, _ = _run_decode_rope(dw, {1, 2, 3}, pos, renumber_from=2)
+    assert_close(res[1], _decode_rope_oracle(dw, 1, pos, oracle.widen(dw.q[1], "bf16")), "bf16")
+    for step in (2, 3):
+        ref = _decode_rope_oracle(dw, step, pos, oracle.widen(dw.q[step], "bf16"), renumber=True)
+        assert_close(res[step], ref, "bf16", max_abs=4e-2 if step == 3 else None)
+
+
+def test_decode_rope_full_size():
+    """14 requests, 20k-90k keys, GQA 64/8 (one CTA reads whole pool rows):
+    256 steps with the append fused; steps 0 and 255 checked in full."""
+    dw = workloads.decode_workload()
+    pos = _rope_positions(dw)
+    res, _, _ = _run_decode_rope(dw, {0, dw.steps - 1}, pos)
+    for step, got in res.items():
+        assert_close(got, _decode_rope_oracle(dw, step, pos, oracle.widen(dw.q[step], "bf16")),
+                     "bf16")
+
+
 def test_tiny_fp32_end_to_end():
     """User 16 / assistant 24 / tool 32 with drop {1:[0], 2:[1]}, reposition
     [2], then 8 decode appends: attention outputs, the active-index list and
