@@ -109,6 +109,25 @@ typedef struct akv_plan akv_plan;
 akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
                            const int32_t *logical_idx, const akv_oplog *ops,
                            akv_plan **plan_out);
+
+/* Plan with shared prefixes (the prefix sharing of the paper review page
+ * section 4.2 radix tree, applied inside one batch: a prefix that several
+ * requests hold identically is computed once).  share_from, share_len: host
+ * [n_req].  share_from[b] = -1: request b shares nothing.  Otherwise
+ * request b's first share_len[b] logical rows are the same tokens as the
+ * first share_len[b] rows of request a = share_from[b] < b, and are not in
+ * the batch: request b owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1, which
+ * carry its logical rows share_len[b] .. T_b-1 (cu_seqlens[b+1] -
+ * cu_seqlens[b] == T_b - share_len[b], T_b = ops[b].msg_start[n_msgs]), and
+ * its rows read the prefix keys from request a's rows.  Conditions
+ * (AKV_ERR_INVALID unless noted): share_len[b] is a message boundary common
+ * to both requests with the same message lengths before it, and a multiple
+ * of 128 (AKV_ERR_UNSUPPORTED otherwise); no drop of either request targets
+ * a message of the prefix; request a shares nothing itself. */
+akv_status akv_plan_create_shared(const akv_shape *shape, int32_t n_req,
+                                  const int32_t *cu_seqlens, const akv_oplog *ops,
+                                  const int32_t *share_from, const int32_t *share_len,
+                                  akv_plan **plan_out);
 void akv_plan_destroy(akv_plan *plan);
 
 typedef struct {

@@ -68,6 +68,9 @@ _SIGS = {
     "akv_version": (ctypes.c_char_p, []),
     "akv_plan_create": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32, _i32p, _i32p,
                                        ctypes.POINTER(OpLog), ctypes.POINTER(ctypes.c_void_p)]),
+    "akv_plan_create_shared": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32, _i32p,
+                                              ctypes.POINTER(OpLog), _i32p, _i32p,
+                                              ctypes.POINTER(ctypes.c_void_p)]),
     "akv_plan_destroy": (None, [ctypes.c_void_p]),
     "akv_plan_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PlanInfo)]),
     "akv_plan_tables": (ctypes.c_int, [ctypes.c_void_p, _i32p, _i32p, _i32p, _i32p]),
@@ -209,16 +212,28 @@ def _stream(stream):
 class Plan:
     """Host plan of a segment-batch restoration prefill (akv_plan_create)."""
 
-    def __init__(self, shp: Shape, cu_seqlens, ops, logical_idx=None):
+    def __init__(self, shp: Shape, cu_seqlens, ops, logical_idx=None, share=None):
+        """share: None, or per request (from, length) -- request b's first
+        `length` logical rows are request `from`'s and are not in the batch
+        (akv_plan_create_shared); (-1, 0) for a request that shares nothing."""
         self._lib = lib()
         self.shape = shp
         self._ops = _Ops(ops)
         cu = _i32(cu_seqlens)
         li = None if logical_idx is None else _i32(logical_idx)
         h = ctypes.c_void_p()
-        _check(self._lib.akv_plan_create(ctypes.byref(shp), len(ops), cu.ctypes.data_as(_i32p),
-                                         None if li is None else li.ctypes.data_as(_i32p),
-                                         self._ops.base, ctypes.byref(h)))
+        if share is None:
+            _check(self._lib.akv_plan_create(ctypes.byref(shp), len(ops),
+                                             cu.ctypes.data_as(_i32p),
+                                             None if li is None else li.ctypes.data_as(_i32p),
+                                             self._ops.base, ctypes.byref(h)))
+        else:
+            sf = _i32([f for f, _ in share])
+            sl = _i32([n for _, n in share])
+            _check(self._lib.akv_plan_create_shared(ctypes.byref(shp), len(ops),
+                                                    cu.ctypes.data_as(_i32p), self._ops.base,
+                                                    sf.ctypes.data_as(_i32p),
+                                                    sl.ctypes.data_as(_i32p), ctypes.byref(h)))
         self.handle = h
         info = PlanInfo()
         _check(self._lib.akv_plan_get_info(h, ctypes.byref(info)))

@@ -150,18 +150,25 @@ struct Group {  // run of permuted slots sharing one drop segment
   int32_t begin, end, dseg;
 };
 
-// Plan one request: tables for rows [c0, c0+T) and its query tiles.
-void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
+// Plan one request: tables for its stored rows and its query tiles.  The
+// request's logical rows are 0..T-1; with a shared prefix of Ps rows (held
+// by another request whose key slots start at owner_c0) only rows Ps..T-1
+// are stored, at batch rows c0..c0+T-Ps-1, and its query tiles read the
+// prefix keys through full windows over the owner's first slots.
+void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o, int64_t Ps = 0,
+                  int64_t owner_c0 = 0) {
   const int n = o->n_msgs;
   const int32_t *ms = o->msg_start;
   const int64_t T = ms[n];
+  const int64_t Tst = T - Ps;  // stored rows
   std::vector<std::vector<int>> drops_at(n);
   std::vector<char> repos_at(n, 0);
   for (int i = 0; i < o->n_drops; ++i) drops_at[o->drop_after[i]].push_back(o->drop_target[i]);
   for (int i = 0; i < o->n_repos; ++i) repos_at[o->repos_after[i]] = 1;
 
-  int32_t *tpos = P->tok_pos.data() + c0, *tseg = P->tok_seg.data() + c0;
-  int32_t *tver = P->tok_ver.data() + c0, *dseg = P->drop_seg.data() + c0;
+  std::vector<int32_t> tpos_v(T), tseg_v(T), tver_v(T), dseg_v(T);
+  int32_t *tpos = tpos_v.data(), *tseg = tseg_v.data(), *tver = tver_v.data(),
+          *dseg = dseg_v.data();
   std::vector<char> alive(n, 0);
   std::vector<int32_t> msg_dseg(n, INT32_MAX);
   // positions per version: version 0 and every repos
@@ -178,7 +185,7 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
       tseg[t] = seg;
       tver[t] = ver;
       // row t sees the active cache at its start plus its own message prefix
-      P->visible_pairs += n_active + (t - a) + 1;
+      if (t >= Ps) P->visible_pairs += n_active + (t - a) + 1;
     }
     alive[m] = 1;
     n_active += b - a;
@@ -208,6 +215,12 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
   P->n_segments += n_seg;
   for (int m = 0; m < n; ++m)
     for (int64_t u = ms[m]; u < ms[m + 1]; ++u) dseg[u] = msg_dseg[m];
+  for (int64_t t = Ps; t < T; ++t) {  // stored rows
+    P->tok_pos[c0 + t - Ps] = tpos[t];
+    P->tok_seg[c0 + t - Ps] = tseg[t];
+    P->tok_ver[c0 + t - Ps] = tver[t];
+    P->drop_seg[c0 + t - Ps] = dseg[t];
+  }
 
   // permuted slot order: messages by decreasing drop segment, then logical order
   std::vector<int> morder(n);
@@ -215,20 +228,20 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
   std::stable_sort(morder.begin(), morder.end(),
                    [&](int x, int y) { return msg_dseg[x] > msg_dseg[y]; });
   std::vector<Group> groups;
-  std::vector<int32_t> u_of(T);  // local slot -> local row
+  std::vector<int32_t> u_of(Tst);  // local slot -> local (logical) row
   {
     int64_t j = 0;
     for (int m : morder) {
-      if (ms[m + 1] == ms[m]) continue;
+      if (ms[m + 1] == ms[m] || ms[m] < Ps) continue;  // empty, or in the shared prefix
       if (groups.empty() || groups.back().dseg != msg_dseg[m])
         groups.push_back({(int32_t)j, (int32_t)j, msg_dseg[m]});
       for (int64_t u = ms[m]; u < ms[m + 1]; ++u) u_of[j++] = (int32_t)u;
       groups.back().end = (int32_t)j;
     }
   }
-  for (int64_t j = 0; j < T; ++j) {
-    P->slot_src[c0 + j] = (int32_t)(c0 + u_of[j]);
-    P->slot_u[c0 + j] = (int32_t)(c0 + u_of[j]);
+  for (int64_t j = 0; j < Tst; ++j) {
+    P->slot_src[c0 + j] = (int32_t)(c0 + u_of[j] - Ps);
+    P->slot_u[c0 + j] = (int32_t)(c0 + u_of[j] - Ps);
     P->slot_dseg[c0 + j] = dseg[u_of[j]];
     for (int v = 0; v < P->max_ver; ++v) {
       int32_t p = v < n_ver ? vpos[v][u_of[j]] : -1;
@@ -238,12 +251,12 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
 
   // query tiles: per version, consecutive rows, 128 at a time
   for (int v = 0; v < n_ver; ++v) {
-    int64_t r0 = ms[ver_first_msg[v]];
+    int64_t r0 = std::max<int64_t>(Ps, ms[ver_first_msg[v]]);
     int64_t r1 = (v + 1 < n_ver) ? ms[ver_first_msg[v + 1]] : T;
     for (int64_t t0 = r0; t0 < r1; t0 += kTileQ) {
       const int64_t t1 = std::min<int64_t>(r1, t0 + kTileQ);
       QTile q{};
-      q.t0 = (int32_t)(c0 + t0);
+      q.t0 = (int32_t)(c0 + t0 - Ps);
       q.len = (int32_t)(t1 - t0);
       q.ver = v;
       q.req = req;
@@ -251,6 +264,12 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
       q.pm_off = (int32_t)P->mwin.size();
       q.seg_lo = tseg[t0];
       q.seg_hi = tseg[t1 - 1];
+      // the shared prefix: never dropped, before every stored row, Ps a
+      // multiple of 128 -> full windows over the owner's first slots
+      for (int64_t a = 0; a < Ps; a += kTileK) {
+        P->windows.push_back((uint32_t)(owner_c0 + a) | kWinFull);
+        ++P->n_full;
+      }
       // visible slot intervals, in slot order: groups with dseg > seg_lo, the
       // prefix of each with u <= t1-1
       int64_t cover_end = -1;
@@ -264,7 +283,7 @@ void plan_request(akv_plan *P, int req, int64_t c0, const akv_oplog *o) {
         while (a < b) {
           // full if every slot of [a, a+128) is in this request, in groups
           // that outlive the tile, and not after the tile's first row
-          bool full = a + kTileK <= T;
+          bool full = a + kTileK <= Tst;
           if (full) {
             int64_t s = a;
             const Group *gp = &g;
@@ -393,9 +412,48 @@ const char *akv_last_error(void) { return g_err.c_str(); }
 
 const char *akv_version(void) { return "akv-gb300 0.1 (sm_103a)"; }
 
-akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
-                           const int32_t *logical_idx, const akv_oplog *ops,
-                           akv_plan **plan_out) {
+}  // extern "C"
+
+namespace {
+// Shared prefix of request b (0 if none): validated against its owner.
+akv_status check_share(int32_t n_req, const int32_t *cu_seqlens, const akv_oplog *ops,
+                       const int32_t *share_from, const int32_t *share_len, int b,
+                       int64_t *Ps) {
+  *Ps = 0;
+  if (!share_from || share_from[b] < 0) return AKV_OK;
+  const int a = share_from[b];
+  const int64_t L = share_len ? share_len[b] : 0;
+  if (a >= b) return fail(AKV_ERR_INVALID, "request %d shares from %d: must be an earlier request", b, a);
+  if (share_from[a] >= 0)
+    return fail(AKV_ERR_INVALID, "request %d shares from %d, which itself shares a prefix", b, a);
+  if (L <= 0 || L % kTileK)
+    return fail(AKV_ERR_UNSUPPORTED, "request %d: shared length %lld must be a positive multiple of %d",
+                b, (long long)L, kTileK);
+  const akv_oplog &ob = ops[b], &oa = ops[a];
+  int m_end = -1;  // the shared prefix is messages 0..m_end-1 in both requests
+  for (int m = 0; m <= ob.n_msgs && m <= oa.n_msgs; ++m) {
+    if (ob.msg_start[m] != oa.msg_start[m]) break;
+    if (ob.msg_start[m] == L) { m_end = m; break; }
+  }
+  if (m_end < 0)
+    return fail(AKV_ERR_INVALID, "request %d: shared length %lld is not a common message boundary of requests %d and %d",
+                b, (long long)L, b, a);
+  for (const akv_oplog *o : {&ob, &oa})
+    for (int i = 0; i < o->n_drops; ++i)
+      if (o->drop_target[i] < m_end)
+        return fail(AKV_ERR_INVALID, "request %d: a shared prefix message (%d) is dropped", b,
+                    o->drop_target[i]);
+  if (L > oa.msg_start[oa.n_msgs] || (int64_t)cu_seqlens[a + 1] - cu_seqlens[a] != oa.msg_start[oa.n_msgs])
+    return fail(AKV_ERR_INVALID, "request %d: owner %d must store all its rows", b, a);
+  *Ps = L;
+  (void)n_req;
+  return AKV_OK;
+}
+
+akv_status plan_create_impl(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                            const int32_t *logical_idx, const akv_oplog *ops,
+                            const int32_t *share_from, const int32_t *share_len,
+                            akv_plan **plan_out) {
   if (akv_status f = injected_fault("akv_plan_create")) return f;
   if (!plan_out) return fail(AKV_ERR_INVALID, "plan_out is NULL");
   *plan_out = nullptr;
@@ -403,19 +461,28 @@ akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t 
   if (n_req < 0 || (n_req > 0 && (!cu_seqlens || !ops)))
     return fail(AKV_ERR_INVALID, "bad request batch");
   if (n_req > 0 && cu_seqlens[0] != 0) return fail(AKV_ERR_INVALID, "cu_seqlens[0] != 0");
+  std::vector<int64_t> shared(n_req, 0);
   for (int b = 0; b < n_req; ++b) {
     if (cu_seqlens[b + 1] < cu_seqlens[b])
       return fail(AKV_ERR_INVALID, "cu_seqlens decreases at %d", b);
-    if (akv_status st = check_oplog(&ops[b], cu_seqlens[b + 1] - cu_seqlens[b], b)) return st;
+    if (akv_status st = check_oplog(&ops[b], -1, b)) return st;
+    if (akv_status st = check_share(n_req, cu_seqlens, ops, share_from, share_len, b, &shared[b]))
+      return st;
+    const int64_t Tb = ops[b].msg_start[ops[b].n_msgs];
+    if ((int64_t)cu_seqlens[b + 1] - cu_seqlens[b] != Tb - shared[b])
+      return fail(AKV_ERR_INVALID, "request %d: messages hold %lld tokens, %lld shared, rows %lld",
+                  b, (long long)Tb, (long long)shared[b],
+                  (long long)(cu_seqlens[b + 1] - cu_seqlens[b]));
   }
   const int64_t T = n_req ? cu_seqlens[n_req] : 0;
   if (T >= (int64_t)INT32_MAX - kSlotPad) return fail(AKV_ERR_UNSUPPORTED, "too many rows");
   if (logical_idx)
     for (int b = 0; b < n_req; ++b)
       for (int64_t i = cu_seqlens[b]; i < cu_seqlens[b + 1]; ++i)
-        if (logical_idx[i] != i - cu_seqlens[b])
+        if (logical_idx[i] != i - cu_seqlens[b] + shared[b])
           return fail(AKV_ERR_INVALID, "row %lld carries logical index %d, expected %lld",
-                      (long long)i, logical_idx[i], (long long)(i - cu_seqlens[b]));
+                      (long long)i, logical_idx[i],
+                      (long long)(i - cu_seqlens[b] + shared[b]));
   akv_plan *P = new (std::nothrow) akv_plan;
   if (!P) return fail(AKV_ERR_INVALID, "host allocation failed");
   P->shape = *shape;
@@ -437,7 +504,16 @@ akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t 
     P->slot_u.assign(T + kSlotPad, INT32_MAX);
     P->slot_dseg.assign(T + kSlotPad, INT32_MIN);
     P->slot_pos.assign((size_t)T * max_ver, 0);
-    for (int b = 0; b < n_req; ++b) plan_request(P, b, cu_seqlens[b], &ops[b]);
+    for (int b = 0; b < n_req; ++b)
+      plan_request(P, b, cu_seqlens[b], &ops[b], shared[b],
+                   shared[b] ? cu_seqlens[share_from[b]] : 0);
+    // a shared prefix is never dropped and precedes every other token, so its
+    // keys sit at positions 0..Ps-1 in every key version of every sharer
+    for (int b = 0; b < n_req; ++b)
+      if (shared[b])
+        for (int v = 0; v < max_ver; ++v)
+          for (int64_t j = 0; j < shared[b]; ++j)
+            P->slot_pos[(size_t)v * T + cu_seqlens[share_from[b]] + j] = (int32_t)j;
     P->order.resize(P->qtiles.size());
     std::iota(P->order.begin(), P->order.end(), 0);
     std::stable_sort(P->order.begin(), P->order.end(), [&](int x, int y) {
@@ -450,6 +526,24 @@ akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t 
   layout_workspace(P);
   *plan_out = P;
   return AKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+akv_status akv_plan_create(const akv_shape *shape, int32_t n_req, const int32_t *cu_seqlens,
+                           const int32_t *logical_idx, const akv_oplog *ops,
+                           akv_plan **plan_out) {
+  return plan_create_impl(shape, n_req, cu_seqlens, logical_idx, ops, nullptr, nullptr, plan_out);
+}
+
+akv_status akv_plan_create_shared(const akv_shape *shape, int32_t n_req,
+                                  const int32_t *cu_seqlens, const akv_oplog *ops,
+                                  const int32_t *share_from, const int32_t *share_len,
+                                  akv_plan **plan_out) {
+  if (!share_from || !share_len) return fail(AKV_ERR_INVALID, "share_from/share_len is NULL");
+  return plan_create_impl(shape, n_req, cu_seqlens, nullptr, ops, share_from, share_len,
+                          plan_out);
 }
 
 void akv_plan_destroy(akv_plan *plan) { delete plan; }

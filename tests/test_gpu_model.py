@@ -93,6 +93,45 @@ def run_decoder(mw, reqs=None):
     return out.cpu().numpy()
 
 
+def run_decoder_shared(mw, prefix):
+    """Forward with the first request owning the shared prefix and the others
+    holding only their rows after it; returns fp32 numpy [stored rows, d]."""
+    torch = _torch()
+    T, n = mw.T, mw.n_req
+    shp = akv.shape(mw.Hq, mw.Hkv, mw.D, "bf16", mw.rope_base)
+    ops = [(mw.msg_start, *mw.ops[b]) for b in range(n)]
+    lens = [T] + [T - prefix] * (n - 1)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    plan = akv.Plan(shp, cu, ops, share=[(-1, 0)] + [(0, prefix)] * (n - 1))
+    x = _bf16(np.concatenate([mw.x] + [mw.x[prefix:]] * (n - 1)))
+    out = torch.empty((int(cu[-1]), mw.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.empty(akv.akv_decoder_workspace(plan, mw.d_model, mw.d_ff), dtype=torch.uint8,
+                     device="cuda")
+    weights = _gpu_weights(mw)
+    akv.akv_decoder_forward(plan, weights, mw.d_model, mw.d_ff, mw.eps, x, out, ws)
+    torch.cuda.synchronize()
+    del weights
+    assert akv.akv_workspace_status(ws) == 0, "a kernel barrier wait timed out"
+    return out.cpu().numpy(), cu
+
+
+def _check_shared_equals_unshared(mw, prefix, full):
+    got, cu = run_decoder_shared(mw, prefix)
+    T = mw.T
+    assert np.array_equal(got[:T], full[:T])
+    for b in range(1, mw.n_req):
+        assert np.array_equal(got[cu[b]:cu[b + 1]], full[b * T + prefix:(b + 1) * T]), b
+
+
+def test_decoder_shared_prefix_small():
+    """The 128-token shared prefix computed once: every stored row equals the
+    unshared forward bit for bit (the prefix keys are the same windows in the
+    same order)."""
+    mw = workloads.model_workload(seed=5, n_req=3, prefix=128, following=640,
+                                  asst_len=(20, 60), tool_len=(60, 150))
+    _check_shared_equals_unshared(mw, 128, run_decoder(mw))
+
+
 def _rel(got, ref):
     d = got - ref
     return float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(ref * ref))), float(np.abs(d).max())
@@ -116,8 +155,9 @@ def test_decoder_small_vs_oracle():
 def test_decoder_full_size_properties():
     """32 requests x (8192 shared + 24576 diverging) tokens: every request's
     shared-prefix rows are bit-identical, a request alone equals the same
-    request inside the batch bit for bit, and the first 1024 prefix rows
-    match the oracle."""
+    request inside the batch bit for bit, the batch with the prefix computed
+    once (akv_plan_create_shared) equals it bit for bit, and the first 1024
+    prefix rows match the oracle."""
     mw = workloads.model_workload()
     T, P = mw.T, 8192
     got = run_decoder(mw)
@@ -127,6 +167,7 @@ def test_decoder_full_size_properties():
         assert np.array_equal(got[b * T:b * T + P], pref), b
     alone = run_decoder(mw, reqs=[5])
     assert np.array_equal(alone, got[5 * T:6 * T])
+    _check_shared_equals_unshared(mw, P, got)  # the prefix computed once
     n = 1024
     ref = oracle.model_replay(mw.weights, mw.x[:n], np.array([0, n], np.int32), [], [], [],
                               mw.Hq, mw.Hkv, mw.D, mw.rope_base, mw.eps)

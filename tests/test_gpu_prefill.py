@@ -2,6 +2,7 @@
 import numpy as np
 import pytest
 
+import kv_cache_drop_gb300 as akv
 import workloads
 from _util import BF16_PEAKY_MAX_ABS, assert_close, oracle_rows, run_prefill, sample_rows
 
@@ -96,3 +97,47 @@ def test_prefill_repos_full_size():
     rows = np.unique(np.concatenate([rows, [b - 1, b, b + 1, b + 200]]))
     assert_close(got[rows], oracle_rows(r, rows), "bf16")
     assert np.isfinite(got).all()
+
+
+def _run_plan(plan, reqs, rows_of, dtype="bf16"):
+    """Run a plan over the given per-request row ranges of the requests'
+    Q/K/V; returns out [T, Hq, D] float32."""
+    torch = _torch_mod()
+    q = akv.to_device(np.concatenate([r.q[a:b] for r, (a, b) in zip(reqs, rows_of)]), dtype)
+    k = akv.to_device(np.concatenate([r.k[a:b] for r, (a, b) in zip(reqs, rows_of)]), dtype)
+    v = akv.to_device(np.concatenate([r.v[a:b] for r, (a, b) in zip(reqs, rows_of)]), dtype)
+    out = torch.zeros_like(q)
+    ws = plan.workspace()
+    akv.akv_segment_attention_run(plan, q, k, v, out, ws)
+    torch.cuda.synchronize()
+    assert akv.akv_workspace_status(ws) == 0
+    return out.float().cpu().numpy()
+
+
+def _torch_mod():
+    import torch
+    return torch
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_shared_prefix_equals_unshared(dtype):
+    """Requests sharing a 256-token first message, computed once: the sharers'
+    remaining rows equal, bit for bit, the same rows of an unshared batch
+    (same windows, same order), and match the oracle."""
+    P = 256
+    rs = workloads.shared_prefix_batch(4, 3, P, 7, 400, dtype=dtype)
+    shp = akv.shape(4, 2, 64, dtype)
+    ops = [r.ops() for r in rs]
+    cu_u = np.concatenate([[0], np.cumsum([r.T for r in rs])])
+    out_u = _run_plan(akv.Plan(shp, cu_u, ops), rs, [(0, r.T) for r in rs], dtype)
+    lens = [rs[0].T] + [r.T - P for r in rs[1:]]
+    cu_s = np.concatenate([[0], np.cumsum(lens)])
+    plan_s = akv.Plan(shp, cu_s, ops, share=[(-1, 0)] + [(0, P)] * (len(rs) - 1))
+    out_s = _run_plan(plan_s, rs, [(0, rs[0].T)] + [(P, r.T) for r in rs[1:]], dtype)
+    for b in range(len(rs)):
+        su = slice(cu_u[b] + (P if b else 0), cu_u[b + 1])
+        ss = slice(cu_s[b], cu_s[b + 1])
+        assert np.array_equal(out_s[ss], out_u[su]), b
+    for b in (1, 2):
+        ref = oracle_rows(rs[b])
+        assert_close(out_s[cu_s[b]:cu_s[b + 1]], ref[P:], dtype)

@@ -135,3 +135,64 @@ def test_workspace_queries_are_host_only(akv):
     assert ws == plan.info["workspace_bytes"] > 0
     assert akv.akv_decode_workspace(shp, 14, 90000) > 0
     assert akv.akv_compact_workspace(r.ops(), r.T) > 0
+
+
+INVALID, UNSUPPORTED = 1, 4
+
+
+def _shared_batch(seed=3, n_req=3, prefix=256):
+    rs = workloads.shared_prefix_batch(seed, n_req, prefix, 6, 300)
+    return rs, [r.ops() for r in rs]
+
+
+def test_shared_prefix_plan_tables_match_unshared(akv):
+    """A sharer's stored rows carry exactly the tables its rows have in an
+    unshared plan, and the visible-pair count drops by the prefix rows'."""
+    rs, ops = _shared_batch()
+    P = 256
+    shp = akv.shape(4, 2, 64, "bf16")
+    cu_u = np.concatenate([[0], np.cumsum([r.T for r in rs])])
+    plan_u = akv.Plan(shp, cu_u, ops)
+    lens = [rs[0].T] + [r.T - P for r in rs[1:]]
+    cu_s = np.concatenate([[0], np.cumsum(lens)])
+    share = [(-1, 0)] + [(0, P)] * (len(rs) - 1)
+    plan_s = akv.Plan(shp, cu_s, ops, share=share)
+    tu, ts = plan_u.tables(), plan_s.tables()
+    for b in range(len(rs)):
+        rows_u = np.arange(cu_u[b] + (P if b else 0), cu_u[b + 1])
+        rows_s = np.arange(cu_s[b], cu_s[b + 1])
+        for name in tu:
+            np.testing.assert_array_equal(ts[name][rows_s], tu[name][rows_u], err_msg=name)
+    # the skipped rows: prefix rows of the sharers, each sees its own prefix
+    skipped = (len(rs) - 1) * P * (P + 1) // 2
+    assert plan_s.info["visible_pairs"] == plan_u.info["visible_pairs"] - skipped
+    assert plan_s.info["T"] == cu_s[-1]
+
+
+def test_shared_prefix_plan_rejects_bad_sharing(akv):
+    rs, ops = _shared_batch()
+    shp = akv.shape(4, 2, 64, "bf16")
+    P = 256
+
+    def cu_for(lens):
+        return np.concatenate([[0], np.cumsum(lens)])
+
+    ok = [rs[0].T, rs[1].T - P, rs[2].T - P]
+    cases = [
+        ([(-1, 0), (0, 200), (-1, 0)], [rs[0].T, rs[1].T - 200, rs[2].T], UNSUPPORTED),
+        ([(-1, 0), (2, P), (-1, 0)], ok[:2] + [rs[2].T], INVALID),  # later owner
+        ([(-1, 0), (0, P), (1, P)], ok, INVALID),                     # owner shares
+        ([(-1, 0), (0, P), (-1, 0)], [rs[0].T, rs[1].T, rs[2].T], INVALID),  # rows
+        ([(-1, 0), (0, 384), (-1, 0)], [rs[0].T, rs[1].T - 384, rs[2].T], INVALID),
+    ]
+    for share, lens, code in cases:
+        with pytest.raises(akv.AkvError) as e:
+            akv.Plan(shp, cu_for(lens), ops, share=share)
+        assert e.value.status == code, (share, e.value)
+    # a drop of a prefix message
+    bad = list(ops)
+    ms, da, dt, ra = bad[1]
+    bad[1] = (ms, np.append(da, 2).astype(np.int32), np.append(dt, 0).astype(np.int32), ra)
+    with pytest.raises(akv.AkvError) as e:
+        akv.Plan(shp, cu_for(ok), bad, share=[(-1, 0), (0, P), (0, P)])
+    assert e.value.status == INVALID

@@ -16,6 +16,7 @@ from .gen import (  # noqa: F401
     rolling_drop_config,
     repos_config,
     decode_workload,
+    shared_prefix_batch,
     model_workload,
     random_request,
 )

@@ -242,6 +242,36 @@ def random_request(seed: int, n_msgs: int, max_len: int, Hq: int = 4, Hkv: int =
     return t
 
 
+def shared_prefix_batch(seed: int, n_req: int, prefix: int, n_msgs: int, max_len: int,
+                        Hq: int = 4, Hkv: int = 2, D: int = 64, dtype: str = "bf16",
+                        p_drop: float = 0.3, p_repos: float = 0.2) -> list:
+    """Requests that start with the same ``prefix``-token message (identical
+    Q/K/V rows), then diverge: their own message lengths U{1..max_len}, drops
+    of later messages only (each at a random boundary at or after its end),
+    repos at random boundaries."""
+    out = []
+    pre = None
+    for b in range(n_req):
+        rng = _streams(seed * 7919 + b, 1)[0]
+        lens = [prefix] + [int(x) for x in rng.integers(1, max_len + 1, size=n_msgs - 1)]
+        msg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        drops, repos = [], []
+        for m in range(1, n_msgs):
+            if rng.random() < p_drop:
+                drops.append((int(rng.integers(m, n_msgs)), m))
+        for m in range(n_msgs):
+            if rng.random() < p_repos:
+                repos.append(m)
+        t = _trajectory(f"shared_{b}", seed * 100 + b, msg_start, ["msg"] * n_msgs, drops, repos,
+                        Hq, Hkv, D, dtype)
+        if pre is None:
+            pre = (t.q[:prefix].copy(), t.k[:prefix].copy(), t.v[:prefix].copy())
+        else:
+            t.q[:prefix], t.k[:prefix], t.v[:prefix] = pre
+        out.append(t)
+    return out
+
+
 @dataclass
 class DecodeWorkload:
     """B requests decoding over a page-size-1 pool.
