@@ -537,14 +537,66 @@ def cpu_baseline(traj, seconds: float, seed: int = 0):
                 seconds=el, threads_note="numpy/BLAS threads of one process")
 
 
+def tree_part(agents=14, rounds=100, seed=21):
+    """Host cost of the cache-history tree in an agent-serving loop: every
+    round each agent's history grows by an assistant and a tool message
+    (rolling drop of tool responses, a repos past 96k positions); the round's
+    request is matched, the previous one finished, the new one inserted; the
+    tree evicts a fixed budget every 10 rounds."""
+    import kv_cache_drop_gb300 as akv
+    import workloads
+    rng = np.random.default_rng(seed)
+    hist = []
+    for a in range(agents):
+        ms, _, drops, repos = workloads.agent_trajectory(seed + a, rounds=rounds,
+                                                         repos_threshold=98304)
+        tok = rng.integers(0, 50000, size=int(ms[-1]), dtype=np.int32)
+        hist.append((np.asarray(ms, np.int32), drops, repos, tok))
+    tree = akv.Tree()
+    kinds = {}
+    t_match = t_ins = 0.0
+    prev = {}
+    n_ops = 0
+    rid = 0
+    for r in range(1, rounds + 1):
+        for a, (ms, drops, repos, tok) in enumerate(hist):
+            n = min(2 * r, len(ms) - 1)
+            da = np.array([x for x, _ in drops if x < n], np.int32)
+            dt = np.array([y for x, y in drops if x < n], np.int32)
+            ra = np.array([x for x in repos if x < n], np.int32)
+            ops = (ms[:n + 1], da, dt, ra)
+            t0 = time.perf_counter()
+            m = tree.match(ops, tok[:ms[n]])
+            t1 = time.perf_counter()
+            if a in prev:
+                tree.finish(prev[a])
+            rid += 1
+            tree.insert(ops, tok[:ms[n]], rid)
+            t2 = time.perf_counter()
+            prev[a] = rid
+            t_match += t1 - t0
+            t_ins += t2 - t1
+            kinds[m["kind"]] = kinds.get(m["kind"], 0) + 1
+            n_ops += 1
+        if r % 10 == 0:
+            tree.evict(200000)
+    st = tree.stats()
+    return dict(agents=agents, rounds=rounds, requests=n_ops,
+                match_us=1e6 * t_match / n_ops, finish_insert_us=1e6 * t_ins / n_ops,
+                kinds=kinds, nodes=st["nodes"], resident_tokens=st["resident_tokens"],
+                note="host C++ through ctypes; histories up to ~110k tokens per agent")
+
+
 def run_ours(args, rank, world):
     import torch
     import kv_cache_drop_gb300 as akv
     import workloads
     akv.lib()
     pk = peaks()
-    if args.part in ("repos", "decode", "decoder"):  # one secondary workload alone
-        if args.part == "repos":
+    if args.part in ("repos", "decode", "decoder", "tree"):  # one secondary workload alone
+        if args.part == "tree":
+            res = tree_part()
+        elif args.part == "repos":
             res = repos_part(workloads.repos_config(), args.steps, args.warmup)
             res["batch"] = repos_batch_part(workloads.decode_workload(), args.steps, args.warmup)
         elif args.part == "decode":
@@ -589,6 +641,7 @@ def run_ours(args, rank, world):
         dec["attn_frac_of_measured_sustained"] = dec["attn_tflops"] / pk["bf16_sus"]
         dec["ffn_gemm_frac_of_measured_sustained"] = dec["ffn_gemm_tflops"] / pk["bf16_sus"]
         parts["decoder_4layer_32req"] = dec
+        parts["cache_tree_14agents"] = tree_part()
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup,
@@ -669,7 +722,8 @@ def main():
                     help="agent rounds of the headline trajectory (100 = the benchmark "
                          "workload; fewer only for small profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
-    ap.add_argument("--part", default="all", choices=["all", "repos", "decode", "decoder"],
+    ap.add_argument("--part", default="all",
+                    choices=["all", "repos", "decode", "decoder", "tree"],
                     help="run one secondary workload alone (for profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -206,6 +206,71 @@ akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *a
                        size_t workspace_bytes, akv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Cache-history tree and drop-aware eviction (paper review page section
+ * 4.2: a radix tree whose paths carry the cache-operation history with the
+ * tokens -- drop nodes record removed entries, a repos opens a branch of
+ * re-numbered positions; eviction frees KV only when no running request
+ * uses it, dropped entries before finished requests' entries, tree nodes
+ * kept as placeholders, each position version separately; section 3.4 /
+ * Figure 5: equal surviving tokens can hold different KV).  Host only: the
+ * tree records which KV exists, the caller owns the KV itself.
+ *
+ * A history is an op log plus token_ids (host int32 [msg_start[n_msgs]],
+ * the messages' token ids).  A message node stands for the KV of that
+ * message computed after exactly the history on its path; a boundary's
+ * drops (as a set) and repos form one operation node.  Storage units: each
+ * message node's own KV, and at each repos node a re-rotated copy of every
+ * message alive there (the new position version).
+ *
+ * akv_tree_match: how much of a new request's history is cached.
+ *   matched_msgs: leading messages whose node exists (same tokens after the
+ *   same history).  A full match continues from the active cache at the end
+ *   of the history; a partial one prefills messages matched_msgs.. over the
+ *   messages alive when the first of them starts.  Of those needed
+ *   messages' tokens: reuse_tokens have a resident copy at the right
+ *   positions (copied as is), rotate_tokens (full match only) only at other
+ *   positions (converted by key rotation), restore_tokens none (evicted).
+ *   prefill_tokens: tokens of the unmatched messages.  kind: RESTORE if any
+ *   needed KV was evicted (one segment-batch prefill restores the state),
+ *   else PREFILL_SUFFIX for a partial match, else ROTATE if some KV needs
+ *   rotation, else REUSE.
+ * akv_tree_insert: the request now runs with this history; its whole path
+ *   exists and is resident.  The newest copy of each message active at the
+ *   end is pinned by the request; every unit on the path is marked dropped
+ *   or not by this request's history.  request_id must not be running.
+ * akv_tree_finish: the request ended; its pins are released.
+ * akv_tree_evict: frees (marks not resident) unpinned units until `tokens`
+ *   tokens are freed or none is left: dropped units first, then by the
+ *   insert that last held them (oldest first), then by creation order.
+ *   *freed: tokens freed.
+ * Errors: AKV_ERR_INVALID for NULL arguments, a bad op log or an unknown /
+ * duplicate request_id. */
+typedef struct akv_tree akv_tree;
+typedef enum {
+  AKV_TREE_REUSE = 0,
+  AKV_TREE_ROTATE = 1,
+  AKV_TREE_PREFILL_SUFFIX = 2,
+  AKV_TREE_RESTORE = 3
+} akv_tree_kind;
+typedef struct {
+  int32_t kind; /* akv_tree_kind */
+  int32_t matched_msgs;
+  int64_t reuse_tokens, rotate_tokens, restore_tokens, prefill_tokens;
+} akv_tree_match_result;
+typedef struct {
+  int64_t nodes, running, resident_tokens, pinned_tokens;
+} akv_tree_stats_t;
+akv_status akv_tree_create(akv_tree **out);
+void akv_tree_destroy(akv_tree *tree);
+akv_status akv_tree_match(const akv_tree *tree, const akv_oplog *ops, const int32_t *token_ids,
+                          akv_tree_match_result *result);
+akv_status akv_tree_insert(akv_tree *tree, const akv_oplog *ops, const int32_t *token_ids,
+                           int64_t request_id);
+akv_status akv_tree_finish(akv_tree *tree, int64_t request_id);
+akv_status akv_tree_evict(akv_tree *tree, int64_t tokens, int64_t *freed);
+akv_status akv_tree_stats(const akv_tree *tree, akv_tree_stats_t *stats);
+
+/* ------------------------------------------------------------------------
  * Repos / position-version conversion (section 3.3, section 4.2 and
  * Appendix A.1.2): for j in 0..r-1, K_out[j] = R(pos_to[j] - pos_from[j]) *
  * K_in[src_idx[j]] and V_out[j] = V_in[src_idx[j]] (values are copied

@@ -61,6 +61,25 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd")]
 
 
+class TreeMatch(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("matched_msgs", ctypes.c_int32),
+                ("reuse_tokens", ctypes.c_int64), ("rotate_tokens", ctypes.c_int64),
+                ("restore_tokens", ctypes.c_int64), ("prefill_tokens", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class TreeStats(ctypes.Structure):
+    _fields_ = [("nodes", ctypes.c_int64), ("running", ctypes.c_int64),
+                ("resident_tokens", ctypes.c_int64), ("pinned_tokens", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+TREE_KINDS = {0: "reuse", 1: "rotate", 2: "prefill_suffix", 3: "restore"}
+
 _lib = None
 
 _SIGS = {
@@ -72,6 +91,16 @@ _SIGS = {
                                               ctypes.POINTER(OpLog), _i32p, _i32p,
                                               ctypes.POINTER(ctypes.c_void_p)]),
     "akv_plan_destroy": (None, [ctypes.c_void_p]),
+    "akv_tree_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p)]),
+    "akv_tree_destroy": (None, [ctypes.c_void_p]),
+    "akv_tree_match": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(OpLog), _i32p,
+                                      ctypes.POINTER(TreeMatch)]),
+    "akv_tree_insert": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(OpLog), _i32p,
+                                       ctypes.c_int64]),
+    "akv_tree_finish": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64]),
+    "akv_tree_evict": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.POINTER(ctypes.c_int64)]),
+    "akv_tree_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(TreeStats)]),
     "akv_plan_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PlanInfo)]),
     "akv_plan_tables": (ctypes.c_int, [ctypes.c_void_p, _i32p, _i32p, _i32p, _i32p]),
     "akv_segment_attention_run": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 5 +
@@ -207,6 +236,56 @@ def _stream(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+class Tree:
+    """Cache-history tree with drop-aware eviction (akv_tree_*).  A history
+    is (ops, token_ids): an op log tuple as for Plan and the messages' token
+    ids (int32, msg_start[-1] of them)."""
+
+    def __init__(self):
+        self._lib = lib()
+        h = ctypes.c_void_p()
+        _check(self._lib.akv_tree_create(ctypes.byref(h)))
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            self._lib.akv_tree_destroy(self.handle)
+            self.handle = None
+
+    @staticmethod
+    def _args(ops, token_ids):
+        o = _Ops([ops])
+        tok = _i32(token_ids)
+        return o, tok
+
+    def match(self, ops, token_ids) -> dict:
+        o, tok = self._args(ops, token_ids)
+        r = TreeMatch()
+        _check(self._lib.akv_tree_match(self.handle, o.ptr(), tok.ctypes.data_as(_i32p),
+                                        ctypes.byref(r)))
+        d = r.as_dict()
+        d["kind"] = TREE_KINDS[d["kind"]]
+        return d
+
+    def insert(self, ops, token_ids, request_id: int):
+        o, tok = self._args(ops, token_ids)
+        _check(self._lib.akv_tree_insert(self.handle, o.ptr(), tok.ctypes.data_as(_i32p),
+                                         request_id))
+
+    def finish(self, request_id: int):
+        _check(self._lib.akv_tree_finish(self.handle, request_id))
+
+    def evict(self, tokens: int) -> int:
+        f = ctypes.c_int64(0)
+        _check(self._lib.akv_tree_evict(self.handle, tokens, ctypes.byref(f)))
+        return f.value
+
+    def stats(self) -> dict:
+        st = TreeStats()
+        _check(self._lib.akv_tree_stats(self.handle, ctypes.byref(st)))
+        return st.as_dict()
 
 
 class Plan:

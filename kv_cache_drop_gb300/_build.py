@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libakv.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
-SOURCES = ["api.cpp", "prep.cu", "attn_simt.cu", "attn_tc.cu", "repos.cu", "compact.cu",
+SOURCES = ["api.cpp", "cache_tree.cpp", "prep.cu", "attn_simt.cu", "attn_tc.cu", "repos.cu", "compact.cu",
            "decode.cu", "gemm.cu", "norm.cu"]
 
 

@@ -83,6 +83,15 @@ struct RopeTheta {
 
 void rope_theta(float base, RopeTheta *out);
 
+// ---- host helpers shared by the C-ABI translation units (api.cpp) ----
+// Records the message returned by akv_last_error and returns st.
+akv_status report_error(akv_status st, const char *fmt, ...);
+// Validates an op log (msg_start CSR, drop/repos boundaries and targets);
+// T < 0 skips the row-count check.
+akv_status validate_oplog(const akv_oplog *o, int64_t T, int req);
+// AKV_FAULT injection for host tests (AKV_OK when not injected).
+akv_status fault_point(const char *entry);
+
 // ---- launchers (defined in the .cu files) ----
 cudaError_t launch_prep(const PlanDev &p, const void *q, const void *k, const void *v,
                         const RopeTheta &th, cudaStream_t s);

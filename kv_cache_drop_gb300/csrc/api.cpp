@@ -414,6 +414,19 @@ const char *akv_version(void) { return "akv-gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"
 
+namespace akv {
+akv_status report_error(akv_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  return fail(st, "%s", buf);
+}
+akv_status validate_oplog(const akv_oplog *o, int64_t T, int req) { return check_oplog(o, T, req); }
+akv_status fault_point(const char *entry) { return injected_fault(entry); }
+}  // namespace akv
+
 namespace {
 // Shared prefix of request b (0 if none): validated against its owner.
 akv_status check_share(int32_t n_req, const int32_t *cu_seqlens, const akv_oplog *ops,
