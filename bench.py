@@ -196,7 +196,7 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
     flops = float(info["visible_pairs"]) * 4 * 64 * traj.Hq
     res = dict(plan=info, plan_host_ms=plan_ms, prep_ms=prep_ms, attn_ms=attn_ms,
                device_ms_total=dev_ms, wall_s=wall, flops_per_step=flops, status=status,
-               clocks=clk.summary(), launches_per_step=3)
+               clocks=clk.summary(), launches_per_step=4)
     if with_e2e:
         # end to end: pinned host inputs -> device, host planning, prefill,
         # device -> host outputs, every step
@@ -372,7 +372,12 @@ def decode_part(dw, warmup_steps=8):
     out = torch.empty((dw.B, dw.Hq, 64), dtype=kp.dtype, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def one(st):
+    def one(st):  # append fused into the decode launch
+        akv.akv_decode_attention_append(shp, dw.B, st["q"], st["pos"], st["kn"], st["vn"],
+                                        st["slots"], kp, vp, st["indptr"], st["idx"], max_kv,
+                                        out, ws)
+
+    def one_separate(st):
         akv.akv_append_kv(shp, dw.B, st["kn"], st["vn"], st["pos"], st["slots"], kp, vp)
         akv.akv_decode_attention(shp, dw.B, st["q"], st["pos"], kp, vp, st["indptr"], st["idx"],
                                  max_kv, out, ws)
@@ -387,6 +392,14 @@ def decode_part(dw, warmup_steps=8):
         ev[s + 1].record(stream)
     torch.cuda.synchronize()
     per_step = [ev[s].elapsed_time(ev[s + 1]) for s in range(dw.steps)]
+    # the same steps as two calls (akv_append_kv, akv_decode_attention)
+    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(dw.steps + 1)]
+    ev2[0].record(stream)
+    for s in range(dw.steps):
+        one_separate(steps[s])
+        ev2[s + 1].record(stream)
+    torch.cuda.synchronize()
+    ms_sep = float(np.sum([ev2[s].elapsed_time(ev2[s + 1]) for s in range(dw.steps)]))
     row = dw.Hkv * 64 * kp.element_size()
     n_total = sum(st["n"] for st in steps)
     bytes_total = n_total * (2 * row + 4) + dw.steps * dw.B * (2 * dw.Hq * 64 * 2 + 2 * row)
@@ -425,7 +438,11 @@ def decode_part(dw, warmup_steps=8):
     torch.cuda.empty_cache()
     return dict(B=dw.B, steps=dw.steps, ms_total=ms, ms_per_step=ms / dw.steps,
                 bytes_per_step=bytes_total / dw.steps, gbs=bytes_total / ms / 1e6,
-                active_entries_per_step=n_total / dw.steps, launches_per_step=3,
+                active_entries_per_step=n_total / dw.steps, launches_per_step=1,
+                memsets_per_step=1,
+                separate_calls=dict(ms_per_step=ms_sep / dw.steps,
+                                    gbs=bytes_total / ms_sep / 1e6, launches_per_step=2,
+                                    note="akv_append_kv + akv_decode_attention"),
                 rotate_on_read=dict(ms_per_step=ms_rope / dw.steps,
                                     bytes_per_step=bytes_rope / dw.steps,
                                     gbs=bytes_rope / ms_rope / 1e6, launches_per_step=2,

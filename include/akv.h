@@ -307,13 +307,27 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
  * rotated).  q_pos, kv_indptr ([B+1]), kv_indices: device int32.  max_kv:
  * host, an upper bound on any request's length (sizes the split-KV grid).
  * out [B, Hq, D] device.  A request with no keys gets zeros.
- * Limit: B <= 65535 (AKV_ERR_UNSUPPORTED). */
+ * Limits: B <= 65535; bf16: max_kv <= 2,048,000 (AKV_ERR_UNSUPPORTED). */
 size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
 akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
                                 const int32_t *q_pos, const void *k_pool, const void *v_pool,
                                 const int32_t *kv_indptr, const int32_t *kv_indices,
                                 int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
                                 akv_stream_t stream);
+
+/* Decode with the step's append fused (one launch for append + decode +
+ * split merge): request b's new token -- raw k_new[b] (device [B, Hkv, D]),
+ * v_new[b] -- is written into pool slot new_slot[b] (device int32 [B]),
+ * its key rotated at q_pos[b] exactly as akv_append_kv would, before the
+ * request's keys are read; kv_indices of request b must end with
+ * new_slot[b].  Otherwise as akv_decode_attention (same workspace size). */
+akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const void *q,
+                                       const int32_t *q_pos, const void *k_new,
+                                       const void *v_new, const int32_t *new_slot, void *k_pool,
+                                       void *v_pool, const int32_t *kv_indptr,
+                                       const int32_t *kv_indices, int32_t max_kv, void *out,
+                                       void *workspace, size_t workspace_bytes,
+                                       akv_stream_t stream);
 
 /* Decode with rotation on read (the fused append and in-kernel repos of a
  * serving step; paper review page section 3.3: a key moves between positions

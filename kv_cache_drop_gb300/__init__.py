@@ -130,6 +130,10 @@ _SIGS = {
                                           ctypes.c_int32, ctypes.c_int32] +
                            [ctypes.c_void_p] * 4 + [_i32p, ctypes.c_void_p, ctypes.c_size_t,
                                                     ctypes.c_void_p]),
+    "akv_decode_attention_append": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
+                                    [ctypes.c_void_p] * 9 + [ctypes.c_int32, ctypes.c_void_p,
+                                                             ctypes.c_void_p, ctypes.c_size_t,
+                                                             ctypes.c_void_p]),
     "akv_decode_rope_workspace": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int32,
                                                     ctypes.c_int32]),
     "akv_decode_attention_rope": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int32] +
@@ -434,6 +438,19 @@ def akv_decode_attention(shp: Shape, B: int, q, q_pos, k_pool, v_pool, kv_indptr
                                       _dev(out), _dev(workspace),
                                       0 if workspace is None else workspace.numel(),
                                       _stream(stream)))
+
+
+def akv_decode_attention_append(shp: Shape, B: int, q, q_pos, k_new, v_new, new_slot, k_pool,
+                                v_pool, kv_indptr, kv_indices, max_kv: int, out, workspace,
+                                stream=None):
+    """Append the step's token (key rotated at q_pos) and decode, one launch."""
+    _check(lib().akv_decode_attention_append(ctypes.byref(shp), B, _dev(q), _dev(q_pos),
+                                             _dev(k_new), _dev(v_new), _dev(new_slot),
+                                             _dev(k_pool), _dev(v_pool), _dev(kv_indptr),
+                                             _dev(kv_indices), max_kv, _dev(out),
+                                             _dev(workspace),
+                                             0 if workspace is None else workspace.numel(),
+                                             _stream(stream)))
 
 
 def akv_decode_rope_workspace(shp: Shape, B: int, max_kv: int) -> int:

@@ -127,6 +127,13 @@ cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *ac
 int compact_blocks(int T);
 
 size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope = false);
+// partials + the per-(request, KV head) merge counters of the bf16 kernel
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv);
+cudaError_t launch_decode_append(int dtype, int B, int Hq, int Hkv, const void *q,
+                                 const int32_t *qpos, const void *k_new, const void *v_new,
+                                 const int32_t *new_slot, void *kp, void *vp,
+                                 const int32_t *indptr, const int32_t *indices, int max_kv,
+                                 void *out, void *ws, const RopeTheta &th, cudaStream_t s);
 cudaError_t launch_decode_rope(int dtype, int B, int Hq, int Hkv, const void *q,
                                const int32_t *qpos, const void *k_new, const void *v_new,
                                const int32_t *new_slot, void *kp, void *vp, const int32_t *indptr,
@@ -147,6 +154,9 @@ cudaError_t launch_widen(int64_t n, const void *x, float *y, cudaStream_t s);
 
 // Decode with its split-KV partials in a static device array (no workspace).
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+// bf16 decode: the in-kernel split merge keeps one weight per split and query
+// head of a group in shared memory (<= 1000 splits of 2048 keys)
+constexpr int kDecodeMaxKeys = 1000 * 2048;
 cudaError_t decode_static_scratch(void **ptr);
 cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *q,
                                  const int32_t *qpos, const void *kp, const void *vp,

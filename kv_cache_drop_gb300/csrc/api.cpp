@@ -899,7 +899,7 @@ akv_status akv_append_kv(const akv_shape *shape, int32_t n, const void *k_new, c
 
 size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv) {
   if (!shape || B < 0 || max_kv < 0 || shape->Hkv <= 0 || shape->Hq % shape->Hkv) return 0;
-  return decode_partials_bytes(B, shape->Hq, max_kv);
+  return decode_workspace_bytes(B, shape->Hq, shape->Hkv, max_kv);
 }
 
 akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
@@ -916,7 +916,9 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
     return fail(AKV_ERR_INVALID, "NULL argument");
   if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
     return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
-  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv);
+  if (shape->dtype == AKV_BF16 && max_kv > kDecodeMaxKeys)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to %d keys per request", kDecodeMaxKeys);
+  const size_t need = decode_workspace_bytes(B, shape->Hq, shape->Hkv, max_kv);
   if (need && (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need))
     return fail(AKV_ERR_WORKSPACE, "decode workspace: need %zu aligned bytes", need);
   RopeTheta th;
@@ -925,6 +927,37 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
                                 kv_indptr, kv_indices, max_kv, out, workspace, th,
                                 (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
+  return AKV_OK;
+}
+
+akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const void *q,
+                                       const int32_t *q_pos, const void *k_new,
+                                       const void *v_new, const int32_t *new_slot, void *k_pool,
+                                       void *v_pool, const int32_t *kv_indptr,
+                                       const int32_t *kv_indices, int32_t max_kv, void *out,
+                                       void *workspace, size_t workspace_bytes,
+                                       akv_stream_t stream) {
+  if (akv_status f = injected_fault("akv_decode_attention_append")) return f;
+  if (akv_status st = check_shape(shape)) return st;
+  if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
+  if (B == 0) return AKV_OK;
+  if (!q || !q_pos || !k_new || !v_new || !new_slot || !k_pool || !v_pool || !kv_indptr ||
+      !out || (max_kv > 0 && !kv_indices))
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
+  if (shape->dtype == AKV_BF16 && max_kv > kDecodeMaxKeys)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to %d keys per request", kDecodeMaxKeys);
+  const size_t need = decode_workspace_bytes(B, shape->Hq, shape->Hkv, max_kv);
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
+    return fail(AKV_ERR_WORKSPACE, "decode workspace: need %zu aligned bytes", need);
+  RopeTheta th;
+  rope_theta(shape->rope_base, &th);
+  cudaError_t e = launch_decode_append(shape->dtype, B, shape->Hq, shape->Hkv, q, q_pos, k_new,
+                                       v_new, new_slot, k_pool, v_pool, kv_indptr, kv_indices,
+                                       max_kv, out, workspace, th, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode with append");
   return AKV_OK;
 }
 
@@ -952,6 +985,8 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
     return fail(AKV_ERR_INVALID, "k_new, v_new and new_slot are given together or not at all");
   if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
     return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
+  if (shape->dtype == AKV_BF16 && max_kv > kDecodeMaxKeys)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to %d keys per request", kDecodeMaxKeys);
   if (shape->dtype == AKV_BF16 && shape->Hkv > 8 && shape->Hkv % 8)
     return fail(AKV_ERR_UNSUPPORTED, "bf16 rotate-on-read decode needs Hkv <= 8 or a multiple of 8");
   const size_t need = decode_partials_bytes(B, shape->Hq, max_kv, true);
@@ -980,7 +1015,9 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
     return fail(AKV_ERR_INVALID, "NULL argument");
   if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)
     return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
-  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv);
+  if (shape->dtype == AKV_BF16 && max_kv > kDecodeMaxKeys)
+    return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to %d keys per request", kDecodeMaxKeys);
+  const size_t need = decode_workspace_bytes(B, shape->Hq, shape->Hkv, max_kv);
   if (need > kStaticScratchBytes)
     return fail(AKV_ERR_UNSUPPORTED,
                 "akv_decode_attention_static: B=%d, Hq=%d, max_kv=%d need %zu bytes of split-KV "

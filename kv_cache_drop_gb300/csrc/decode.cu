@@ -87,11 +87,18 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Each CTA also counts itself done for its (request, KV head); the last one
+// merges the group's split partials and writes the output (no separate
+// combine launch).  With new_slot, the CTA that owns a request's last key
+// first appends the step's token: K rotated at q_pos (the same rotation
+// table as the query) and V, into pool slot new_slot[b].
 __global__ void __launch_bounds__(kWarps * 32)
     decode_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
-                       const int32_t *__restrict__ qpos, const __nv_bfloat16 *__restrict__ kp,
-                       const __nv_bfloat16 *__restrict__ vp, const int32_t *__restrict__ indptr,
-                       const int32_t *__restrict__ indices, Partials part, RopeTheta th) {
+                       const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
+                       const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                       Partials part, RopeTheta th, int *counters, __nv_bfloat16 *out,
+                       const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                       const int32_t *new_slot) {
   // dynamic smem: per warp kStages x (K tile 2 KiB + V tile 2 KiB); reused
   // for the merge of the warps' partials
   extern __shared__ __align__(128) uint8_t smem[];
@@ -103,10 +110,28 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int gid = lane >> 2, tig = lane & 3;
   const int beg = indptr[b], n = indptr[b + 1] - beg;
   const int c0 = split * kChunk, c1 = min(n, c0 + kChunk);
-  if (c0 >= n) return;  // the combine reads only the splits that hold keys
+  if (c0 >= n) {  // the merge reads only the splits that hold keys
+    if (n <= 0 && split == 0)  // a request with no keys gets zeros
+      for (int i = threadIdx.x; i < grp * kD; i += blockDim.x)
+        out[((int64_t)b * Hq + g * grp) * kD + i] = __float2bfloat16_rn(0.f);
+    return;
+  }
 
   if (threadIdx.x < kD / 2) rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
   __syncthreads();
+  if (new_slot && c1 == n) {  // fused append of the step's token (head g)
+    const int64_t src = ((int64_t)b * Hkv + g) * kD, dst = ((int64_t)new_slot[b] * Hkv + g) * kD;
+    if (threadIdx.x < kD / 2) {
+      const int f = threadIdx.x;
+      const float x1 = __bfloat162float(k_new[src + f]), x2 = __bfloat162float(k_new[src + f + kD / 2]);
+      kp[dst + f] = __float2bfloat16_rn(x1 * cs[f] - x2 * sn[f]);
+      kp[dst + f + kD / 2] = __float2bfloat16_rn(x1 * sn[f] + x2 * cs[f]);
+    } else if (threadIdx.x < kD / 2 + kD / 8) {
+      const int c = threadIdx.x - kD / 2;
+      reinterpret_cast<uint4 *>(vp + dst)[c] = reinterpret_cast<const uint4 *>(v_new + src)[c];
+    }
+    __syncthreads();  // the appended row is visible to this CTA's gathers
+  }
 
   // Q fragments (A operand, rows = query heads of the group, 16 rows padded
   // with zeros), rotated at the query position; 1/sqrt(D) * log2(e) folded in.
@@ -316,6 +341,59 @@ __global__ void __launch_bounds__(kWarps * 32)
       part.ml[2 * pi] = M;
       part.ml[2 * pi + 1] = L;
     }
+  }
+  // the last CTA of (request, KV head) to finish merges the splits
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  const int used = min(ns, (n + kChunk - 1) / kChunk);
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(counters + (int64_t)b * Hkv + g, 1);
+    is_last = prev == used - 1;
+    if (is_last) counters[(int64_t)b * Hkv + g] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // merge: per query head (row) the split weights 2^(m_s - M) / L go to
+  // shared memory (reusing the tile buffers), then every output element is
+  // a weighted sum over the splits with all its loads in flight.
+  float *wgt = reinterpret_cast<float *>(smem);  // [16 rows][used]
+  float *rowl = wgt + 16 * used;                 // [16]
+  for (int i = threadIdx.x; i < grp * used; i += kWarps * 32) {
+    const int row = i / used, sp = i % used;
+    wgt[row * used + sp] = __ldcg(part.ml + 2 * (((int64_t)b * Hq + g * grp + row) * ns + sp));
+  }
+  __syncthreads();
+  if (threadIdx.x < grp) {
+    const int row = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < used; ++sp) M = fmaxf(M, wgt[row * used + sp]);
+    const float Mr = M == -INFINITY ? 0.f : M;
+    float L = 0.f;
+    for (int sp = 0; sp < used; ++sp) {
+      const float f = exp2f(wgt[row * used + sp] - Mr);
+      L += __ldcg(part.ml + 2 * (((int64_t)b * Hq + g * grp + row) * ns + sp) + 1) * f;
+      wgt[row * used + sp] = f;
+    }
+    rowl[row] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < grp * kD; idx += kWarps * 32) {
+    const int row = idx / kD, col = idx % kD;
+    const float *po = part.o + ((int64_t)b * Hq + g * grp + row) * ns * kD + col;
+    const float *w = wgt + row * used;
+    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= used; sp += 4) {
+      x0 += __ldcg(po + (int64_t)sp * kD) * w[sp];
+      x1 += __ldcg(po + (int64_t)(sp + 1) * kD) * w[sp + 1];
+      x2 += __ldcg(po + (int64_t)(sp + 2) * kD) * w[sp + 2];
+      x3 += __ldcg(po + (int64_t)(sp + 3) * kD) * w[sp + 3];
+    }
+    for (; sp < used; ++sp) x0 += __ldcg(po + (int64_t)sp * kD) * w[sp];
+    out[((int64_t)b * Hq + g * grp + row) * kD + col] =
+        __float2bfloat16_rn(((x0 + x1) + (x2 + x3)) * rowl[row]);
   }
 }
 
@@ -801,6 +879,48 @@ size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope) {
   return ml + o;
 }
 
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv) {
+  return decode_partials_bytes(B, Hq, max_kv) + ((size_t)B * Hkv * 4 + 255) / 256 * 256;
+}
+
+namespace {
+// bf16 decode over a workspace laid out as partials then merge counters
+cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qpos, void *kp,
+                        void *vp, const int32_t *indptr, const int32_t *indices, int max_kv,
+                        void *out, void *ws, const RopeTheta &th, const void *k_new,
+                        const void *v_new, const int32_t *new_slot, cudaStream_t s) {
+  const int ns = n_splits(max_kv);
+  Partials part = partials(ws, B, Hq, max_kv);
+  int *counters = reinterpret_cast<int *>(static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv));
+  constexpr int smem = kWarps * kStages * 4096;
+  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // the merge counters start at zero (the kernel also leaves them at zero)
+  e = cudaMemsetAsync(counters, 0, (size_t)B * Hkv * 4, s);
+  if (e != cudaSuccess) return e;
+  decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
+      Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
+      indices, part, th, counters, (__nv_bfloat16 *)out, (const __nv_bfloat16 *)k_new,
+      (const __nv_bfloat16 *)v_new, new_slot);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_decode_append(int dtype, int B, int Hq, int Hkv, const void *q,
+                                 const int32_t *qpos, const void *k_new, const void *v_new,
+                                 const int32_t *new_slot, void *kp, void *vp,
+                                 const int32_t *indptr, const int32_t *indices, int max_kv,
+                                 void *out, void *ws, const RopeTheta &th, cudaStream_t s) {
+  if (dtype == AKV_BF16)
+    return decode_bf16(B, Hq, Hkv, q, qpos, kp, vp, indptr, indices, max_kv, out, ws, th, k_new,
+                       v_new, new_slot, s);
+  cudaError_t e = launch_append(dtype, Hkv, B, k_new, v_new, qpos, new_slot, kp, vp, th, s);
+  if (e != cudaSuccess) return e;
+  return launch_decode(dtype, B, Hq, Hkv, q, qpos, kp, vp, indptr, indices, max_kv, out, ws, th,
+                       s);
+}
+
 cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, const int32_t *qpos,
                           const void *kp, const void *vp, const int32_t *indptr,
                           const int32_t *indices, int max_kv, void *out, void *ws,
@@ -808,20 +928,8 @@ cudaError_t launch_decode(int dtype, int B, int Hq, int Hkv, const void *q, cons
   const int ns = n_splits(max_kv);
   Partials part = partials(ws, B, Hq, max_kv);
   if (dtype == AKV_BF16) {
-    constexpr int smem = kWarps * kStages * 4096;
-    static bool attr = false;  // once per process (single device use)
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    dim3 grid(ns, Hkv, B);
-    decode_bf16_kernel<<<grid, kWarps * 32, smem, s>>>(
-        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
-        (const __nv_bfloat16 *)vp, indptr, indices, part, th);
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part,
-                                                                    (__nv_bfloat16 *)out);
+    return decode_bf16(B, Hq, Hkv, q, qpos, const_cast<void *>(kp), const_cast<void *>(vp),
+                       indptr, indices, max_kv, out, ws, th, nullptr, nullptr, nullptr, s);
   } else {
     dim3 grid(ns, Hq, B);
     decode_f32_kernel<<<grid, 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos, (const float *)kp,
@@ -905,14 +1013,8 @@ cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *
   const int ns = n_splits(max_kv);
   Partials part = partials(scratch, B, Hq, max_kv);
   if (dtype == AKV_BF16) {
-    constexpr int smem = kWarps * kStages * 4096;
-    e = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
-        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)kp,
-        (const __nv_bfloat16 *)vp, indptr, indices, part, th);
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part,
-                                                                    (__nv_bfloat16 *)out);
+    return decode_bf16(B, Hq, Hkv, q, qpos, const_cast<void *>(kp), const_cast<void *>(vp),
+                       indptr, indices, max_kv, out, scratch, th, nullptr, nullptr, nullptr, s);
   } else {
     decode_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos,
                                                       (const float *)kp, (const float *)vp,

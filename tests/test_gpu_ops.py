@@ -172,6 +172,55 @@ def _run_decode(dw, check_steps):
     return results
 
 
+def _run_decode_fused(dw, check_steps):
+    """The same steps through akv_decode_attention_append (append fused)."""
+    torch = _torch()
+    shp = akv.shape(dw.Hq, dw.Hkv, 64, dw.dtype)
+    kp = akv.to_device(dw.k_pool, dw.dtype)
+    vp = akv.to_device(dw.v_pool, dw.dtype)
+    max_kv = max(len(a) for a in dw.active_slots) + dw.steps
+    ws = torch.empty(akv.akv_decode_workspace(shp, dw.B, max_kv), dtype=torch.uint8,
+                     device="cuda")
+    results = {}
+    for step in range(dw.steps):
+        indptr, idx = dw.indices_at(step)
+        q = akv.to_device(dw.q[step], dw.dtype)
+        out = torch.empty_like(q)
+        akv.akv_decode_attention_append(
+            shp, dw.B, q, akv.i32_device(dw.L + step), akv.to_device(dw.k_new[step], dw.dtype),
+            akv.to_device(dw.v_new[step], dw.dtype), akv.i32_device(dw.append_slots[step]), kp,
+            vp, akv.i32_device(indptr), akv.i32_device(idx), max_kv, out, ws)
+        if step in check_steps:
+            torch.cuda.synchronize()
+            results[step] = out.float().cpu().numpy()
+    torch.cuda.synchronize()
+    return results, kp, vp
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_fused_append_equals_separate_calls(dtype):
+    """Append fused into the decode launch: outputs and the pool bit-identical
+    to akv_append_kv followed by akv_decode_attention, and close to fp64."""
+    torch = _torch()
+    dw = workloads.decode_workload(seed=14, B=3, active=(100, 5000), steps=3, Hq=8, Hkv=2,
+                                   dtype=dtype)
+    sep = _run_decode(dw, {0, 1, 2})
+    fused, kp, vp = _run_decode_fused(dw, {0, 1, 2})
+    for step in (0, 1, 2):
+        assert np.array_equal(fused[step], sep[step]), step
+        assert_close(fused[step], _decode_oracle(dw, step, oracle.widen(dw.q[step], dtype)), dtype)
+    # the appended rows equal akv_append_kv's, bit for bit
+    shp = akv.shape(dw.Hq, dw.Hkv, 64, dtype)
+    kp2 = akv.to_device(dw.k_pool, dtype)
+    vp2 = akv.to_device(dw.v_pool, dtype)
+    for step in range(dw.steps):
+        akv.akv_append_kv(shp, dw.B, akv.to_device(dw.k_new[step], dtype),
+                          akv.to_device(dw.v_new[step], dtype), akv.i32_device(dw.L + step),
+                          akv.i32_device(dw.append_slots[step]), kp2, vp2)
+    torch.cuda.synchronize()
+    assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_decode_small(dtype):
     dw = workloads.decode_workload(seed=8, B=3, active=(100, 5000), steps=3, Hq=8, Hkv=2,
