@@ -2,7 +2,7 @@
 // page section 4 serving flow: decode reads only the active cache; system
 // README: drop/repos work at page size 1).
 //
-// Split-KV: request b's index list is cut into chunks of kChunk keys; one CTA
+// Split-KV: request b's index list is cut into chunks of `chunk` keys; one CTA
 // takes (chunk, KV head g, request b) and produces a partial (row max m, row
 // sum l, unnormalised output o) for the Hq/Hkv query heads of group g; a
 // combine kernel merges the partials by their log-sum-exp.
@@ -22,11 +22,14 @@
 namespace akv {
 namespace {
 
-constexpr int kChunk = 2048;  // keys per CTA
+constexpr int kChunk = 2048;     // keys per CTA of the fp32 kernel
+constexpr int kMinChunk = 1024;  // bf16: chunk chosen per call in [kMinChunk, kMaxChunk]
+constexpr int kMaxChunk = 4096;
+constexpr int kMaxSplits = 1000;  // bf16: the in-kernel merge's weights fit shared memory
 constexpr int kRChunk = 512;  // keys per CTA of the rotate-on-read kernels (all heads of a block)
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Partials {
@@ -98,7 +101,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                        const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                        Partials part, RopeTheta th, int *counters, __nv_bfloat16 *out,
                        const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
-                       const int32_t *new_slot) {
+                       const int32_t *new_slot, int chunk) {
   // dynamic smem: per warp kStages x (K tile 2 KiB + V tile 2 KiB); reused
   // for the merge of the warps' partials
   extern __shared__ __align__(128) uint8_t smem[];
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int beg = indptr[b], n = indptr[b + 1] - beg;
-  const int c0 = split * kChunk, c1 = min(n, c0 + kChunk);
+  const int c0 = split * chunk, c1 = min(n, c0 + chunk);
   if (c0 >= n) {  // the merge reads only the splits that hold keys
     if (n <= 0 && split == 0)  // a request with no keys gets zeros
       for (int i = threadIdx.x; i < grp * kD; i += blockDim.x)
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   __shared__ int is_last;
   __threadfence();
   __syncthreads();
-  const int used = min(ns, (n + kChunk - 1) / kChunk);
+  const int used = min(ns, (n + chunk - 1) / chunk);
   if (threadIdx.x == 0) {
     const int prev = atomicAdd(counters + (int64_t)b * Hkv + g, 1);
     is_last = prev == used - 1;
@@ -873,7 +876,7 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(int Hq, int ns, int 
 }  // namespace
 
 size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope) {
-  const int ns = n_splits(max_kv, rope ? kRChunk : kChunk);
+  const int ns = n_splits(max_kv, rope ? kRChunk : kMinChunk);  // bf16: the most splits
   const size_t ml = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
   const size_t o = ((size_t)B * Hq * ns * kD * 4 + 255) / 256 * 256;
   return ml + o;
@@ -889,8 +892,19 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         void *vp, const int32_t *indptr, const int32_t *indices, int max_kv,
                         void *out, void *ws, const RopeTheta &th, const void *k_new,
                         const void *v_new, const int32_t *new_slot, cudaStream_t s) {
-  const int ns = n_splits(max_kv);
-  Partials part = partials(ws, B, Hq, max_kv);
+  // chunk: the largest of 4096, 2048, 1024 keys that still gives about two
+  // waves of CTAs (4 per SM) when every request is max_kv long
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+  }
+  int chunk = kMaxChunk;
+  while (chunk > kMinChunk && (int64_t)B * n_splits(max_kv, chunk) * Hkv < 2LL * 4 * sms) chunk /= 2;
+  while (n_splits(max_kv, chunk) > kMaxSplits) chunk *= 2;
+  const int ns = n_splits(max_kv, chunk);
+  Partials part = partials(ws, B, Hq, max_kv, chunk);
   int *counters = reinterpret_cast<int *>(static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv));
   constexpr int smem = kWarps * kStages * 4096;
   cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel,
@@ -902,7 +916,7 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
   decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
       Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
       indices, part, th, counters, (__nv_bfloat16 *)out, (const __nv_bfloat16 *)k_new,
-      (const __nv_bfloat16 *)v_new, new_slot);
+      (const __nv_bfloat16 *)v_new, new_slot, chunk);
   return cudaGetLastError();
 }
 }  // namespace
