@@ -445,7 +445,8 @@ def decode_part(dw, warmup_steps=8):
                                     note="akv_append_kv + akv_decode_attention"),
                 rotate_on_read=dict(ms_per_step=ms_rope / dw.steps,
                                     bytes_per_step=bytes_rope / dw.steps,
-                                    gbs=bytes_rope / ms_rope / 1e6, launches_per_step=2,
+                                    gbs=bytes_rope / ms_rope / 1e6, launches_per_step=1,
+                                    memsets_per_step=1,
                                     note="raw-key pool, per-entry positions, append fused"))
 
 

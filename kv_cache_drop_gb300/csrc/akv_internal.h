@@ -129,6 +129,7 @@ int compact_blocks(int T);
 size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope = false);
 // partials + the per-(request, KV head) merge counters of the bf16 kernel
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv);
+size_t decode_rope_workspace_bytes(int dtype, int B, int Hq, int Hkv, int max_kv);
 cudaError_t launch_decode_append(int dtype, int B, int Hq, int Hkv, const void *q,
                                  const int32_t *qpos, const void *k_new, const void *v_new,
                                  const int32_t *new_slot, void *kp, void *vp,

@@ -963,7 +963,7 @@ akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const 
 
 size_t akv_decode_rope_workspace(const akv_shape *shape, int32_t B, int32_t max_kv) {
   if (!shape || B <= 0 || max_kv < 0) return 0;
-  return decode_partials_bytes(B, shape->Hq, max_kv, true);
+  return decode_rope_workspace_bytes(shape->dtype, B, shape->Hq, shape->Hkv, max_kv);
 }
 
 akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const void *q,
@@ -987,9 +987,7 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
     return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to 16 query heads per KV head");
   if (shape->dtype == AKV_BF16 && max_kv > kDecodeMaxKeys)
     return fail(AKV_ERR_UNSUPPORTED, "bf16 decode supports up to %d keys per request", kDecodeMaxKeys);
-  if (shape->dtype == AKV_BF16 && shape->Hkv > 8 && shape->Hkv % 8)
-    return fail(AKV_ERR_UNSUPPORTED, "bf16 rotate-on-read decode needs Hkv <= 8 or a multiple of 8");
-  const size_t need = decode_partials_bytes(B, shape->Hq, max_kv, true);
+  const size_t need = decode_rope_workspace_bytes(shape->dtype, B, shape->Hq, shape->Hkv, max_kv);
   if (need && (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need))
     return fail(AKV_ERR_WORKSPACE, "decode (rotate on read) workspace: need %zu aligned bytes", need);
   RopeTheta th;

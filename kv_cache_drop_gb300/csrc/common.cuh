@@ -28,7 +28,8 @@ __device__ __forceinline__ void rope_cs(double theta, double pos, float *c, floa
 // bits so that k * C1 and k * C2 are exact for |k| < 2^16 (Cody-Waite).  The
 // reduced angle is accurate to ~3e-7 rad.  Larger positions take the double
 // path above.
-__device__ __forceinline__ void rope_cs_pair(float hi, float lo, int pos, float *c, float *s) {
+// pos * theta reduced to about [-pi, pi]
+__device__ __forceinline__ float rope_angle(float hi, float lo, int pos) {
   const float p = (float)pos;  // exact
   const float ah = p * hi;
   const float ae = fmaf(p, hi, -ah);  // exact error of the product
@@ -37,7 +38,10 @@ __device__ __forceinline__ void rope_cs_pair(float hi, float lo, int pos, float 
   float r = fmaf(-k, 6.28125f, ah);            // 2*pi = 6.28125
   r = fmaf(-k, 1.93023681640625e-3f, r);       //      + 1.93023681640625e-3
   r = fmaf(-k, 5.0703633860393888e-6f, r);     //      + 5.07036338...e-6 (+ ~2e-13)
-  sincosf(r + al, s, c);
+  return r + al;
+}
+__device__ __forceinline__ void rope_cs_pair(float hi, float lo, int pos, float *c, float *s) {
+  sincosf(rope_angle(hi, lo, pos), s, c);
 }
 __device__ __forceinline__ void rope_cs(const RopeTheta &th, int f, int pos, float *c, float *s) {
   if (pos < -262144 || pos > 262144) {

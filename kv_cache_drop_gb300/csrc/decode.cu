@@ -26,7 +26,7 @@ constexpr int kChunk = 2048;     // keys per CTA of the fp32 kernel
 constexpr int kMinChunk = 1024;  // bf16: chunk chosen per call in [kMinChunk, kMaxChunk]
 constexpr int kMaxChunk = 4096;
 constexpr int kMaxSplits = 1000;  // bf16: the in-kernel merge's weights fit shared memory
-constexpr int kRChunk = 512;  // keys per CTA of the rotate-on-read kernels (all heads of a block)
+constexpr int kRChunk = 512;  // keys per CTA of the fp32 rotate-on-read kernel
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;
 constexpr int kStages = 2;
@@ -95,17 +95,36 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // combine launch).  With new_slot, the CTA that owns a request's last key
 // first appends the step's token: K rotated at q_pos (the same rotation
 // table as the query) and V, into pool slot new_slot[b].
+//
+// kRope (rotation on read): the pool holds keys before RoPE and kvpos gives
+// each entry's position; a tile's 16 positions arrive with its K/V by
+// cp.async, every lane forms cos/sin for the 16 (key, frequency) pairs of its
+// K fragments (keys gid, gid + 8; the pair (d, d + 32) sits in k-steps ks and
+// ks + 2 of the same lane), rotates them in registers and splits the result
+// into bf16 hi + lo, S = qhi khi + qlo khi + qhi klo.  The append is then a
+// plain copy.
+constexpr int kStageBytes(bool rope) { return rope ? 4096 + 64 : 4096; }
+
+// cos/sin of pos * theta by the fast sin/cos instructions (absolute error
+// about 4e-7 on the reduced angle, |r| <= pi)
+__device__ __forceinline__ void rope_cs_fast(float hi, float lo, int pos, float *c, float *s) {
+  __sincosf(rope_angle(hi, lo, pos), s, c);
+}
+
+template <bool kRope>
 __global__ void __launch_bounds__(kWarps * 32)
     decode_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
                        const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
                        const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                        Partials part, RopeTheta th, int *counters, __nv_bfloat16 *out,
                        const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
-                       const int32_t *new_slot, int chunk) {
-  // dynamic smem: per warp kStages x (K tile 2 KiB + V tile 2 KiB); reused
-  // for the merge of the warps' partials
+                       const int32_t *new_slot, int chunk, const int32_t *__restrict__ kvpos) {
+  // dynamic smem: per warp kStages x (K tile 2 KiB + V tile 2 KiB [+ 16
+  // positions]); reused for the merge of the warps' partials
+  constexpr int kSB = kStageBytes(kRope);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float cs[kD / 2], sn[kD / 2];
+  __shared__ ThetaSmem ts;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int ns = gridDim.x;
   const int grp = Hq / Hkv;
@@ -121,10 +140,19 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 
   if (threadIdx.x < kD / 2) rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
+  if (kRope) stage_theta(th, ts);
   __syncthreads();
   if (new_slot && c1 == n) {  // fused append of the step's token (head g)
     const int64_t src = ((int64_t)b * Hkv + g) * kD, dst = ((int64_t)new_slot[b] * Hkv + g) * kD;
-    if (threadIdx.x < kD / 2) {
+    if (kRope) {  // the pool keeps keys before RoPE: a copy
+      if (threadIdx.x < 2 * (kD / 8)) {
+        const int c = threadIdx.x % (kD / 8);
+        if (threadIdx.x < kD / 8)
+          reinterpret_cast<uint4 *>(kp + dst)[c] = reinterpret_cast<const uint4 *>(k_new + src)[c];
+        else
+          reinterpret_cast<uint4 *>(vp + dst)[c] = reinterpret_cast<const uint4 *>(v_new + src)[c];
+      }
+    } else if (threadIdx.x < kD / 2) {
       const int f = threadIdx.x;
       const float x1 = __bfloat162float(k_new[src + f]), x2 = __bfloat162float(k_new[src + f + kD / 2]);
       kp[dst + f] = __float2bfloat16_rn(x1 * cs[f] - x2 * sn[f]);
@@ -191,7 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
-  uint8_t *wsm = smem + warp * kStages * 4096;
+  uint8_t *wsm = smem + warp * kStages * kSB;
   const uint32_t wsm_u = smem_u32(wsm);
   const int n_tiles = c0 < c1 ? (c1 - c0 + kTileKeys - 1) / kTileKeys : 0;
   // tiles of this warp: warp, warp + kWarps, ...
@@ -203,6 +231,10 @@ __global__ void __launch_bounds__(kWarps * 32)
       int slot = 0;
       const bool have = lane < kTileKeys && k0 + lane < c1;
       if (have) slot = __ldg(indices + beg + k0 + lane);
+      if (kRope && lane < kTileKeys)  // the tile's positions (0 past the end)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(
+                         wsm_u + stage * kSB + 4096 + 4 * lane),
+                     "l"(kvpos + beg + (have ? k0 + lane : 0)), "r"(have ? 4 : 0));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int idx = lane + 32 * i;  // 128 chunks per tile: key = idx/8, chunk = idx%8
@@ -210,8 +242,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int s = __shfl_sync(0xffffffffu, slot, key);
         const bool valid = k0 + key < c1;
         const int64_t off = ((int64_t)s * Hkv + g) * kD + ch * 8;
-        cp_async16(wsm_u + stage * 4096 + swz(key, ch), kp + off, valid);
-        cp_async16(wsm_u + stage * 4096 + 2048 + swz(key, ch), vp + off, valid);
+        cp_async16(wsm_u + stage * kSB + swz(key, ch), kp + off, valid);
+        cp_async16(wsm_u + stage * kSB + 2048 + swz(key, ch), vp + off, valid);
       }
     }
     asm volatile("cp.async.commit_group;\n" ::);
@@ -224,12 +256,60 @@ __global__ void __launch_bounds__(kWarps * 32)
     issue(it + kStages - 1);
     asm volatile("cp.async.wait_group %0;\n" ::"n"(kStages - 1));
     __syncwarp();
-    const uint32_t kt = wsm_u + (it % kStages) * 4096, vt = kt + 2048;
+    const uint32_t kt = wsm_u + (it % kStages) * kSB, vt = kt + 2048;
     const int k0 = c0 + (warp + it * kWarps) * kTileKeys;
-    // S = Q K^T: two n-blocks of 8 keys
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (kRope) {
+      const int32_t *tpos = reinterpret_cast<const int32_t *>(wsm + (it % kStages) * kSB + 4096);
+      const int pa = tpos[gid], pb = tpos[gid + 8];
+      uint32_t kb[4][4], kl[4][4];
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
+      for (int ks = 0; ks < 4; ++ks) {
+        const int mi = lane >> 3;
+        const int key = (mi >> 1) * 8 + (lane & 7);
+        const int ch = ks * 2 + (mi & 1);
+        ldsm_x4(kt + swz(key, ch), kb[ks][0], kb[ks][1], kb[ks][2], kb[ks][3]);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
+          const int pos = (r >> 1) ? pb : pa;
+          const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
+          float c0f, s0f, c1f, s1f;
+          if (pos < -262144 || pos > 262144) {
+            rope_cs(th.th[f], (double)pos, &c0f, &s0f);
+            rope_cs(th.th[f + 1], (double)pos, &c1f, &s1f);
+          } else {
+            rope_cs_fast(ts.hi[f], ts.lo[f], pos, &c0f, &s0f);
+            rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &c1f, &s1f);
+          }
+          __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
+          __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
+          const float x1a = __low2float(a), x1b = __high2float(a);
+          const float x2a = __low2float(bq), x2b = __high2float(bq);
+          const float y1a = x1a * c0f - x2a * s0f, y1b = x1b * c1f - x2b * s1f;
+          const float y2a = x1a * s0f + x2a * c0f, y2b = x1b * s1f + x2b * c1f;
+          kb[ks][r] = pack_bf16(y1a, y1b);
+          kb[ks + 2][r] = pack_bf16(y2a, y2b);
+          const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
+          const __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
+          kl[ks][r] = pack_bf16(y1a - __low2float(h1), y1b - __high2float(h1));
+          kl[ks + 2][r] = pack_bf16(y2a - __low2float(h2), y2b - __high2float(h2));
+        }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+        mma_bf16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+        mma_bf16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+        mma_bf16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+        mma_bf16(s[0], qa[ks], kl[ks][0], kl[ks][1]);
+        mma_bf16(s[1], qa[ks], kl[ks][2], kl[ks][3]);
+      }
+    }
+    // S = Q K^T: two n-blocks of 8 keys
+#pragma unroll
+    for (int ks = 0; ks < 4 && !kRope; ++ks) {
       // matrices: (keys 0-7, d lo), (keys 0-7, d hi), (keys 8-15, d lo), (keys 8-15, d hi)
       const int mi = lane >> 3;
       const int key = (mi >> 1) * 8 + (lane & 7);
@@ -482,279 +562,9 @@ __global__ void __launch_bounds__(128)
 // Decode with rotation on read.  The pool holds keys before RoPE and every
 // index entry carries its position, so a repos only rewrites the positions
 // (4 bytes per entry) instead of moving and re-rotating the keys.  The step's
-// append is fused: the CTA that owns a request's last key (the new token's
-// slot) first copies the new raw K/V rows into the pool.
-//
-// bf16: CTA = (key chunk, block of up to 8 KV heads, request), one warp per
-// KV head, all warps on the same 16-key tiles, so the warps together read
-// the keys' whole pool rows and share one cos/sin table per tile (16 keys x
-// 32 frequencies, built by all threads after the tile's positions land).
-// Each warp rotates its K fragments in registers (pairs d, d + 32 sit in
-// k-steps ks and ks + 2 of the same lane), splits them into bf16 hi + lo,
-// and runs the same tensor-core tile and online softmax as the kernel above.
+// append is fused: the new raw K/V rows are copied into the pool before the
+// keys are read.  bf16 runs decode_bf16_kernel<true> (above).
 // ---------------------------------------------------------------------------
-constexpr int kRWarps = 8;   // KV heads per CTA
-constexpr int kRStages = 4;  // tiles in flight per warp
-constexpr int kRTileBytes = 4096 + 64;  // K tile, V tile, 16 positions
-constexpr int kRTabStride = kD / 2 + 2;  // float2 per key row: 4-way (minimal) bank spread
-constexpr int kRSmem = kRWarps * kRStages * kRTileBytes + 2 * kTileKeys * kRTabStride * 8;
-
-__global__ void __launch_bounds__(kRWarps * 32, 1)
-    decode_rope_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
-                            const int32_t *__restrict__ qpos, const __nv_bfloat16 *k_new,
-                            const __nv_bfloat16 *v_new, const int32_t *new_slot,
-                            __nv_bfloat16 *kp, __nv_bfloat16 *vp,
-                            const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-                            const int32_t *__restrict__ kvpos, Partials part, RopeTheta th) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float qcs[kD / 2], qsn[kD / 2];
-  __shared__ ThetaSmem ts;
-  const int split = blockIdx.x, b = blockIdx.z;
-  const int ns = gridDim.x;
-  const int nw = blockDim.x >> 5;  // KV heads of this CTA
-  const int grp = Hq / Hkv;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = blockIdx.y * kRWarps + warp;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int beg = indptr[b], n = indptr[b + 1] - beg;
-  const int c0 = split * kRChunk, c1 = min(n, c0 + kRChunk);
-  if (c0 >= n) return;  // the combine reads only the splits that hold keys
-
-  stage_theta(th, ts);
-  if (new_slot && c1 == n) {  // fused append: this CTA owns the request's last key
-    const int64_t slot = new_slot[b];
-    for (int i = threadIdx.x; i < nw * 8; i += blockDim.x) {
-      const int gg = blockIdx.y * kRWarps + i / 8, c = i % 8;
-      const int64_t src = ((int64_t)b * Hkv + gg) * kD, dst = (slot * Hkv + gg) * kD;
-      reinterpret_cast<uint4 *>(kp + dst)[c] = reinterpret_cast<const uint4 *>(k_new + src)[c];
-      reinterpret_cast<uint4 *>(vp + dst)[c] = reinterpret_cast<const uint4 *>(v_new + src)[c];
-    }
-  }
-  __syncthreads();  // frequencies staged; appended rows visible to this CTA's gathers
-  if (threadIdx.x < kD / 2) rope_cs(th, ts, threadIdx.x, qpos[b], &qcs[threadIdx.x], &qsn[threadIdx.x]);
-  __syncthreads();
-
-  // query fragments of group g, rotated at the query position, split hi + lo
-  uint32_t qa[4][4], ql[4][4];
-  {
-    const float qs = 0.125f * kLog2e;
-    float qv[2][16];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int row = gid + 8 * hh;
-      const bool ok = row < grp;
-      const __nv_bfloat16 *qrow = q + ((int64_t)b * Hq + g * grp + (ok ? row : 0)) * kD;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
-          qv[hh][ks * 4 + e] = ok ? __bfloat162float(qrow[d]) : 0.f;
-        }
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
-          const float x1 = qv[hh][ks * 4 + e], x2 = qv[hh][(ks + 2) * 4 + e];
-          qv[hh][ks * 4 + e] = (x1 * qcs[d] - x2 * qsn[d]) * qs;
-          qv[hh][(ks + 2) * 4 + e] = (x1 * qsn[d] + x2 * qcs[d]) * qs;
-        }
-    auto lo = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
-      qa[ks][0] = pack_bf16(a0[0], a0[1]);
-      qa[ks][1] = pack_bf16(a1[0], a1[1]);
-      qa[ks][2] = pack_bf16(a0[2], a0[3]);
-      qa[ks][3] = pack_bf16(a1[2], a1[3]);
-      ql[ks][0] = pack_bf16(lo(a0[0]), lo(a0[1]));
-      ql[ks][1] = pack_bf16(lo(a1[0]), lo(a1[1]));
-      ql[ks][2] = pack_bf16(lo(a0[2]), lo(a0[3]));
-      ql[ks][3] = pack_bf16(lo(a1[2]), lo(a1[3]));
-    }
-  }
-
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-  uint8_t *wsm = smem + warp * kRStages * kRTileBytes;
-  const uint32_t wsm_u = smem_u32(wsm);
-  // cos/sin table, double buffered: [buf][key][freq] as (cos, sin)
-  float2 *tab = reinterpret_cast<float2 *>(smem + kRWarps * kRStages * kRTileBytes);
-  const int n_tiles = (c1 - c0 + kTileKeys - 1) / kTileKeys;
-  auto issue = [&](int tile) {
-    const int stage = tile % kRStages;
-    if (tile < n_tiles) {
-      const int k0 = c0 + tile * kTileKeys;
-      int slot = 0;
-      const bool have = lane < kTileKeys && k0 + lane < c1;
-      if (have) slot = __ldg(indices + beg + k0 + lane);
-      if (lane < kTileKeys) {  // this tile's positions (0 past the end)
-        const uint32_t dst = wsm_u + stage * kRTileBytes + 4096 + 4 * lane;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst),
-                     "l"(kvpos + beg + (have ? k0 + lane : 0)), "r"(have ? 4 : 0));
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int idx = lane + 32 * i;  // 128 chunks per tile: key = idx/8, chunk = idx%8
-        const int key = idx >> 3, ch = idx & 7;
-        const int sl = __shfl_sync(0xffffffffu, slot, key);
-        const bool valid = k0 + key < c1;
-        const int64_t off = ((int64_t)sl * Hkv + g) * kD + ch * 8;
-        cp_async16(wsm_u + stage * kRTileBytes + swz(key, ch), kp + off, valid);
-        cp_async16(wsm_u + stage * kRTileBytes + 2048 + swz(key, ch), vp + off, valid);
-      }
-    }
-    asm volatile("cp.async.commit_group;\n" ::);
-  };
-
-#pragma unroll
-  for (int it = 0; it < kRStages - 1; ++it) issue(it);
-  for (int it = 0; it < n_tiles; ++it) {
-    issue(it + kRStages - 1);
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(kRStages - 1));
-    __syncwarp();
-    const int stage = it % kRStages;
-    const uint32_t kt = wsm_u + stage * kRTileBytes, vt = kt + 2048;
-    const int32_t *tpos = reinterpret_cast<const int32_t *>(wsm + stage * kRTileBytes + 4096);
-    float2 *tb = tab + (it & 1) * kTileKeys * kRTabStride;
-    // this CTA's share of the tile's cos/sin table (every warp holds the
-    // same positions)
-    for (int e = threadIdx.x; e < kTileKeys * (kD / 2); e += blockDim.x) {
-      const int key = e / (kD / 2), f = e % (kD / 2);
-      float c, sn;
-      rope_cs(th, ts, f, tpos[key], &c, &sn);
-      tb[key * kRTabStride + f] = make_float2(c, sn);
-    }
-    __syncthreads();
-    const int k0 = c0 + it * kTileKeys;
-    // K fragments of the tile, rotated in registers: lane holds keys gid and
-    // gid + 8, dims 16ks + 2tig + {0, 1} (+8); d < 32 pairs with d + 32
-    uint32_t kb[4][4];
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int mi = lane >> 3;
-      const int key = (mi >> 1) * 8 + (lane & 7);
-      const int ch = ks * 2 + (mi & 1);
-      ldsm_x4(kt + swz(key, ch), kb[ks][0], kb[ks][1], kb[ks][2], kb[ks][3]);
-    }
-    // The rotated key is split like the query, hi = bf16(k), lo = bf16(k - hi),
-    // and S = qhi khi + qlo khi + qhi klo: the scores see the rotated key to
-    // ~16 bits, as if it were exact, at a third more (idle) MMA work.
-    uint32_t kl[4][4];
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
-        const int key = gid + 8 * (r >> 1);
-        const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
-        const float4 cs2 = *reinterpret_cast<const float4 *>(tb + key * kRTabStride + f);  // f, f+1
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
-        __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
-        const float x1a = __low2float(a), x1b = __high2float(a);
-        const float x2a = __low2float(bq), x2b = __high2float(bq);
-        const float y1a = x1a * cs2.x - x2a * cs2.y, y1b = x1b * cs2.z - x2b * cs2.w;
-        const float y2a = x1a * cs2.y + x2a * cs2.x, y2b = x1b * cs2.w + x2b * cs2.z;
-        kb[ks][r] = pack_bf16(y1a, y1b);
-        kb[ks + 2][r] = pack_bf16(y2a, y2b);
-        const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
-        const __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
-        kl[ks][r] = pack_bf16(y1a - __low2float(h1), y1b - __high2float(h1));
-        kl[ks + 2][r] = pack_bf16(y2a - __low2float(h2), y2b - __high2float(h2));
-      }
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      mma_bf16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
-      mma_bf16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
-      mma_bf16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
-      mma_bf16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
-      mma_bf16(s[0], qa[ks], kl[ks][0], kl[ks][1]);
-      mma_bf16(s[1], qa[ks], kl[ks][2], kl[ks][3]);
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + nb * 8 + 2 * tig + (e & 1);
-        if (key >= c1) s[nb][e] = -INFINITY;
-        mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
-      }
-    float alpha[2], mref[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mn = fmaxf(m[r], mx[r]);
-      mref[r] = mn == -INFINITY ? 0.f : mn;
-      alpha[r] = exp2f(m[r] - mref[r]);
-      m[r] = mn;
-    }
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s[nb][e] = exp2f(s[nb][e] - mref[e >> 1]);
-        rs[e >> 1] += s[nb][e];
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + rs[r];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16(s[0][0], s[0][1]);
-    pa[1] = pack_bf16(s[0][2], s[0][3]);
-    pa[2] = pack_bf16(s[1][0], s[1][1]);
-    pa[3] = pack_bf16(s[1][2], s[1][3]);
-#pragma unroll
-    for (int nb2 = 0; nb2 < 4; ++nb2) {
-      const int mi = lane >> 3;
-      const int key = (mi & 1) * 8 + (lane & 7);
-      const int ch = nb2 * 2 + (mi >> 1);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vt + swz(key, ch), v0, v1, v2, v3);
-      mma_bf16(o[2 * nb2], pa, v0, v1);
-      mma_bf16(o[2 * nb2 + 1], pa, v2, v3);
-    }
-    __syncwarp();
-  }
-  asm volatile("cp.async.wait_group 0;\n" ::);
-
-  // one warp per KV head: its rows are final partials
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-  }
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int row = gid + 8 * hh;
-    if (row >= grp) continue;
-    const int64_t pi = ((int64_t)b * Hq + g * grp + row) * ns + split;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<float2 *>(part.o + pi * kD + i * 8 + 2 * tig) =
-          make_float2(o[i][2 * hh], o[i][2 * hh + 1]);
-    if (tig == 0) {
-      part.ml[2 * pi] = m[hh];
-      part.ml[2 * pi + 1] = l[hh];
-    }
-  }
-}
-
 // fp32 with rotation on read: thread per key, block of 128 threads per
 // (split, query head, request).  The new rows are appended by every CTA of
 // the last split before it reads (identical values).
@@ -886,12 +696,18 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv) {
   return decode_partials_bytes(B, Hq, max_kv) + ((size_t)B * Hkv * 4 + 255) / 256 * 256;
 }
 
+size_t decode_rope_workspace_bytes(int dtype, int B, int Hq, int Hkv, int max_kv) {
+  return dtype == AKV_BF16 ? decode_workspace_bytes(B, Hq, Hkv, max_kv)
+                           : decode_partials_bytes(B, Hq, max_kv, true);
+}
+
 namespace {
 // bf16 decode over a workspace laid out as partials then merge counters
 cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qpos, void *kp,
                         void *vp, const int32_t *indptr, const int32_t *indices, int max_kv,
                         void *out, void *ws, const RopeTheta &th, const void *k_new,
-                        const void *v_new, const int32_t *new_slot, cudaStream_t s) {
+                        const void *v_new, const int32_t *new_slot, cudaStream_t s,
+                        const int32_t *kvpos = nullptr) {
   // chunk: the largest of 4096, 2048, 1024 keys that still gives about two
   // waves of CTAs (4 per SM) when every request is max_kv long
   static int sms = 0;
@@ -906,17 +722,18 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
   const int ns = n_splits(max_kv, chunk);
   Partials part = partials(ws, B, Hq, max_kv, chunk);
   int *counters = reinterpret_cast<int *>(static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv));
-  constexpr int smem = kWarps * kStages * 4096;
-  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool rope = kvpos != nullptr;
+  const int smem = kWarps * kStages * kStageBytes(rope);
+  auto kern = rope ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // the merge counters start at zero (the kernel also leaves them at zero)
   e = cudaMemsetAsync(counters, 0, (size_t)B * Hkv * 4, s);
   if (e != cudaSuccess) return e;
-  decode_bf16_kernel<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
+  kern<<<dim3(ns, Hkv, B), kWarps * 32, smem, s>>>(
       Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
       indices, part, th, counters, (__nv_bfloat16 *)out, (const __nv_bfloat16 *)k_new,
-      (const __nv_bfloat16 *)v_new, new_slot, chunk);
+      (const __nv_bfloat16 *)v_new, new_slot, chunk, kvpos);
   return cudaGetLastError();
 }
 }  // namespace
@@ -960,29 +777,13 @@ cudaError_t launch_decode_rope(int dtype, int B, int Hq, int Hkv, const void *q,
                                void *ws, const RopeTheta &th, cudaStream_t s) {
   const int ns = n_splits(max_kv, kRChunk);
   Partials part = partials(ws, B, Hq, max_kv, kRChunk);
-  if (dtype == AKV_BF16) {
-    static bool attr = false;  // once per process (single device use)
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(decode_rope_bf16_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    const int hb = (Hkv + kRWarps - 1) / kRWarps;
-    // every head block has min(Hkv, 8) warps; Hkv is a multiple of 8 or below 8
-    const int nw = Hkv < kRWarps ? Hkv : kRWarps;
-    decode_rope_bf16_kernel<<<dim3(ns, hb, B), nw * 32, kRSmem, s>>>(
-        Hq, Hkv, (const __nv_bfloat16 *)q, qpos, (const __nv_bfloat16 *)k_new,
-        (const __nv_bfloat16 *)v_new, new_slot, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
-        indices, kvpos, part, th);
-    decode_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kRChunk, indptr, part,
-                                                                    (__nv_bfloat16 *)out);
-  } else {
-    decode_rope_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(
-        Hq, Hkv, (const float *)q, qpos, (const float *)k_new, (const float *)v_new, new_slot,
-        (float *)kp, (float *)vp, indptr, indices, kvpos, part, th);
-    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kRChunk, indptr, part, (float *)out);
-  }
+  if (dtype == AKV_BF16)
+    return decode_bf16(B, Hq, Hkv, q, qpos, kp, vp, indptr, indices, max_kv, out, ws, th, k_new,
+                       v_new, new_slot, s, kvpos);
+  decode_rope_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(
+      Hq, Hkv, (const float *)q, qpos, (const float *)k_new, (const float *)v_new, new_slot,
+      (float *)kp, (float *)vp, indptr, indices, kvpos, part, th);
+  decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kRChunk, indptr, part, (float *)out);
   return cudaGetLastError();
 }
 
