@@ -280,15 +280,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (!((vis[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
       }
-      // row max: eight independent 3-input chains, then a short tree
+      // row max: eight independent 3-input chains over columns k8 + 8j
+      // (j = 0-2, then pairs up to j = 14, then j = 15), then a short tree
       float mx8[8];
 #pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8) mx8[k8] = __uint_as_float(sr[k8]);
+      for (int k8 = 0; k8 < 8; ++k8)
+        mx8[k8] = ptx::max3(__uint_as_float(sr[k8]), __uint_as_float(sr[8 + k8]),
+                            __uint_as_float(sr[16 + k8]));
 #pragma unroll
-      for (int c = 8; c < 128; c += 16)
+      for (int c = 24; c + 16 <= 120; c += 16)
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8)
           mx8[k8] = ptx::max3(mx8[k8], __uint_as_float(sr[c + k8]), __uint_as_float(sr[c + 8 + k8]));
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8) mx8[k8] = fmaxf(mx8[k8], __uint_as_float(sr[120 + k8]));
       const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
                              fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx * kScaleLog2);
