@@ -94,7 +94,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qi = p.order[blockIdx.x / n_pairs], pair = blockIdx.x % n_pairs;
+  // head pair major: the CTAs in flight share one KV head's K/V windows,
+  // which then stay in L2; query tiles by decreasing window count within it
+  const int qi = p.order[blockIdx.x % p.n_qtiles], pair = blockIdx.x / p.n_qtiles;
   const QTile qt = p.qtiles[qi];
   const int grp = p.Hq / p.Hkv;
   const int h0 = 2 * pair, g = h0 / grp;
