@@ -15,7 +15,12 @@
  *    "host" pointers are read synchronously during the call and may be
  *    reused as soon as the call returns.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *    stream) and runs asynchronously.  Arguments are validated before any
+ *    stream) and runs asynchronously: a call does not wait for earlier work
+ *    on the stream.  Tables planned on the host are copied to the workspace
+ *    through pinned host blocks that the library allocates on first use and
+ *    keeps for reuse (at most a few, each reused once its copies have
+ *    completed; when all are busy the call waits for the oldest).  Arguments
+ *    are validated before any
  *    launch: on AKV_ERR_INVALID / AKV_ERR_UNSUPPORTED / AKV_ERR_WORKSPACE
  *    nothing was enqueued.  AKV_ERR_CUDA reports a failed runtime call or
  *    launch.  Kernels that wait on barriers do so with an iteration limit;

@@ -23,6 +23,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <numeric>
 #include <string>
@@ -367,14 +368,144 @@ PlanDev device_view(const akv_plan *P, void *ws) {
   return d;
 }
 
+// Host-to-device uploads of tables built on the host.  A cudaMemcpyAsync
+// from pageable memory returns only after the copy has run, i.e. after all
+// earlier work on the stream, so every call would wait for the GPU.  The
+// tables are instead packed into pinned host blocks owned by the library and
+// copied from there asynchronously.  A block is handed out again only once
+// every copy out of it has completed (one event per upload); blocks are
+// kept for reuse and never freed before the process exits.
+struct HostPart {
+  size_t dst_off;  // byte offset from the destination base
+  const void *src;
+  size_t bytes;
+};
+
+class PinnedPool {
+ public:
+  struct Block {
+    char *p = nullptr;
+    size_t bytes = 0;
+    std::vector<cudaEvent_t> pending;  // uploads from this block not yet known complete
+  };
+  // A block of at least `bytes` with no copy in flight; false if pinned
+  // memory cannot be had.  At most kMaxBlocks blocks are allocated: beyond
+  // that the caller waits for the copies out of a block that fits (the host
+  // is then at most a few uploads ahead of the GPU), instead of pinning more
+  // memory (pinning is slow and may synchronise the device).
+  bool acquire(size_t bytes, Block *out) {
+    std::unique_lock<std::mutex> lock(mu_);
+    int best = -1, busy = -1;
+    for (int i = 0; i < (int)free_.size(); ++i) {
+      Block &b = free_[i];
+      prune(&b);
+      if (b.bytes < bytes) continue;
+      if (b.pending.empty()) {
+        if (best < 0 || b.bytes < free_[best].bytes) best = i;
+      } else if (busy < 0) {
+        busy = i;  // the oldest returned block that fits
+      }
+    }
+    if (best < 0 && busy >= 0 && n_alloc_ >= kMaxBlocks) best = busy;
+    if (best >= 0) {
+      *out = std::move(free_[best]);
+      free_.erase(free_.begin() + best);
+      lock.unlock();
+      for (cudaEvent_t e : out->pending) {
+        (void)cudaEventSynchronize(e);
+        cudaEventDestroy(e);
+      }
+      (void)cudaGetLastError();
+      out->pending.clear();
+      return true;
+    }
+    Block b;
+    b.bytes = align_up(std::max<size_t>(bytes, 1), size_t(1) << 20);
+    if (cudaHostAlloc((void **)&b.p, b.bytes, cudaHostAllocPortable) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    ++n_alloc_;
+    *out = std::move(b);
+    return true;
+  }
+  void release(Block b) {
+    std::lock_guard<std::mutex> lock(mu_);
+    free_.push_back(std::move(b));
+  }
+
+ private:
+  static void prune(Block *b) {
+    std::vector<cudaEvent_t> keep;
+    for (cudaEvent_t e : b->pending) {
+      const cudaError_t q = cudaEventQuery(e);
+      if (q == cudaErrorNotReady) {
+        keep.push_back(e);
+      } else {
+        (void)cudaGetLastError();
+        cudaEventDestroy(e);
+      }
+    }
+    b->pending.swap(keep);
+  }
+  static constexpr int kMaxBlocks = 4;
+  std::mutex mu_;
+  std::vector<Block> free_;  // returned blocks, oldest first
+  int n_alloc_ = 0;
+};
+
+PinnedPool &pinned_pool() {
+  static PinnedPool *pool = new PinnedPool();  // never destroyed: blocks may be in use at exit
+  return *pool;
+}
+
+// Copies the parts to dst + dst_off on stream s without waiting for the
+// stream.  Falls back to plain (blocking) copies when no pinned memory can
+// be had.
+cudaError_t upload_async(char *dst, const HostPart *parts, int n, cudaStream_t s) {
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += align_up(parts[i].bytes, 16);
+  PinnedPool::Block blk;
+  if (!pinned_pool().acquire(total, &blk)) {
+    for (int i = 0; i < n; ++i) {
+      if (!parts[i].bytes) continue;
+      cudaError_t e = cudaMemcpyAsync(dst + parts[i].dst_off, parts[i].src, parts[i].bytes,
+                                      cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  size_t o = 0;
+  for (int i = 0; i < n; ++i) {
+    if (parts[i].bytes) std::memcpy(blk.p + o, parts[i].src, parts[i].bytes);
+    o += align_up(parts[i].bytes, 16);
+  }
+  o = 0;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    if (parts[i].bytes)
+      e = cudaMemcpyAsync(dst + parts[i].dst_off, blk.p + o, parts[i].bytes,
+                          cudaMemcpyHostToDevice, s);
+    o += align_up(parts[i].bytes, 16);
+  }
+  cudaEvent_t ev = nullptr;
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventRecord(ev, s);
+  if (e != cudaSuccess) {
+    // copies may be in flight without an event to track them: the block is
+    // not reused (it stays allocated)
+    if (ev) cudaEventDestroy(ev);
+    return e;
+  }
+  blk.pending.push_back(ev);
+  pinned_pool().release(std::move(blk));
+  return cudaSuccess;
+}
+
 akv_status upload_plan(const akv_plan *P, void *ws, cudaStream_t s) {
   char *b = (char *)ws;
   const WsLayout &w = P->ws;
-  struct Part {
-    size_t off;
-    const void *src;
-    size_t bytes;
-  } parts[] = {
+  const HostPart parts[] = {
       {w.tok_qpos, P->tok_pos.data(), 4 * P->tok_pos.size()},
       {w.tok_seg, P->tok_seg.data(), 4 * P->tok_seg.size()},
       {w.slot_src, P->slot_src.data(), 4 * P->slot_src.size()},
@@ -388,11 +519,8 @@ akv_status upload_plan(const akv_plan *P, void *ws, cudaStream_t s) {
   };
   cudaError_t e = cudaMemsetAsync(b + w.status, 0, 256, s);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
-  for (const Part &p : parts) {
-    if (!p.bytes) continue;
-    e = cudaMemcpyAsync(b + p.off, p.src, p.bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
-  }
+  e = upload_async(b, parts, (int)(sizeof(parts) / sizeof(parts[0])), s);
+  if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   return AKV_OK;
 }
 
@@ -769,12 +897,10 @@ akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *a
   size_t o0 = 0, o1 = align_up(4 * (size_t)(ops->n_msgs + 1), 256);
   size_t o2 = o1 + align_up((size_t)ops->n_msgs + 1, 256);
   size_t o3 = o2 + align_up((size_t)ops->n_msgs + 1, 256);
-  cudaError_t e = cudaMemcpyAsync(b + o0, ops->msg_start, 4 * (size_t)(c.n_msgs + 1),
-                                  cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(b + o1, c.keep.data(), c.n_msgs, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(b + o2, c.alive_br.data(), c.n_msgs, cudaMemcpyHostToDevice, s);
+  const HostPart parts[] = {{o0, ops->msg_start, 4 * (size_t)(c.n_msgs + 1)},
+                            {o1, c.keep.data(), (size_t)c.n_msgs},
+                            {o2, c.alive_br.data(), (size_t)c.n_msgs}};
+  cudaError_t e = upload_async(b, parts, 3, s);
   if (e != cudaSuccess) return cuda_fail(e, "compact upload");
   CompactDev d{};
   d.msg_start = (const int32_t *)(b + o0);
@@ -849,7 +975,8 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
   packed.insert(packed.end(), kpos.begin(), kpos.end());
   cudaStream_t s = (cudaStream_t)stream;
   int32_t *b = (int32_t *)workspace;
-  cudaError_t e = cudaMemcpyAsync(b, packed.data(), 4 * packed.size(), cudaMemcpyHostToDevice, s);
+  const HostPart part{0, packed.data(), 4 * packed.size()};
+  cudaError_t e = upload_async((char *)b, &part, 1, s);
   if (e != cudaSuccess) return cuda_fail(e, "repos tables upload");
   RopeTheta th;
   rope_theta(shape->rope_base, &th);
