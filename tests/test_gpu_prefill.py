@@ -141,3 +141,43 @@ def test_shared_prefix_equals_unshared(dtype):
     for b in (1, 2):
         ref = oracle_rows(rs[b])
         assert_close(out_s[cu_s[b]:cu_s[b + 1]], ref[P:], dtype)
+
+
+def test_calls_do_not_wait_for_the_stream():
+    """Host planning and the upload of its tables do not wait for earlier
+    work on the stream: with about a second of GPU work queued ahead, the
+    calls return at once, and their results are right once it has run."""
+    import time
+
+    import torch
+    import oracle
+    r = workloads.random_request(61, n_msgs=6, max_len=200, Hq=8, Hkv=2, dtype="bf16",
+                                 p_drop=0.3, p_repos=0.3, min_len=20)
+    shp = akv.shape(8, 2, 64, "bf16")
+    ops, cu = [r.ops()], [0, r.T]
+    q, k, v = (akv.to_device(x, "bf16") for x in (r.q, r.k, r.v))
+    out = torch.zeros_like(q)
+    ws = torch.empty(akv.akv_segment_attention_workspace(shp, cu, ops), dtype=torch.uint8,
+                     device="cuda")
+    idx = torch.full((r.T,), -1, dtype=torch.int32, device="cuda")
+    pos = torch.full((r.T,), -1, dtype=torch.int32, device="cuda")
+    cws = torch.empty(max(1, akv.akv_compact_workspace(r.ops(), r.T)), dtype=torch.uint8,
+                      device="cuda")
+    akv.akv_segment_attention(shp, cu, None, ops, q, k, v, out, ws)  # first use: set-up
+    akv.akv_compact(r.ops(), r.T, -1, idx, pos, cws)
+    torch.cuda.synchronize()
+    out.zero_()
+    idx.fill_(-1)
+    torch.cuda._sleep(2_000_000_000)  # about a second of spinning on the stream
+    t0 = time.perf_counter()
+    akv.akv_segment_attention(shp, cu, None, ops, q, k, v, out, ws)
+    n = akv.akv_compact(r.ops(), r.T, -1, idx, pos, cws)
+    host_s = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    assert host_s < 0.25, f"the calls waited {host_s:.3f} s for the stream"
+    assert akv.akv_workspace_status(ws) == 0
+    ref, _ = oracle.replay_attention(*r.ops(), r.q, r.k, r.v, "bf16", r.rope_base)
+    assert_close(out.float().cpu().numpy(), ref, "bf16")
+    ou, op = oracle.compact(*r.ops(), upto=-1)
+    np.testing.assert_array_equal(idx[:n].cpu().numpy(), ou)
+    np.testing.assert_array_equal(pos[:n].cpu().numpy(), op)
