@@ -348,8 +348,10 @@ akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const 
  * k_pool/v_pool are written only at those slots.  Workspace: device,
  * 256-byte aligned, akv_decode_rope_workspace() bytes (bf16: split-KV
  * partials and merge counters as for akv_decode_attention; fp32: partials
- * of 512-key chunks).  bf16 keys are rotated in fp32 and the scores use the
- * rotated key split into bf16 hi + lo parts. */
+ * of 512-key chunks).  bf16: keys are rotated in fp32 and rounded to fp16
+ * for the score product, so a rotated key component must stay below 65504
+ * in magnitude (a larger one becomes inf); the query keeps ~22 bits as fp16
+ * hi + lo parts. */
 size_t akv_decode_rope_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
 akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const void *q,
                                      const int32_t *q_pos, const void *k_new, const void *v_new,

@@ -80,6 +80,19 @@ __device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -100,9 +113,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // each entry's position; a tile's 16 positions arrive with its K/V by
 // cp.async, every lane forms cos/sin for the 16 (key, frequency) pairs of its
 // K fragments (keys gid, gid + 8; the pair (d, d + 32) sits in k-steps ks and
-// ks + 2 of the same lane), rotates them in registers and splits the result
-// into bf16 hi + lo, S = qhi khi + qlo khi + qhi klo.  The append is then a
-// plain copy.
+// ks + 2 of the same lane), rotates them in fp32 registers and rounds the
+// result to fp16 (11-bit significand); the query is split into fp16 hi + lo
+// and S = qhi k + qlo k in fp16 MMAs.  Rotated keys must lie within the fp16
+// range (|k| < 65504; a larger one gives inf).  The append is then a plain
+// copy.
 constexpr int kStageBytes(bool rope) { return rope ? 4096 + 64 : 4096; }
 
 // cos/sin of pos * theta by the fast sin/cos instructions (absolute error
@@ -112,7 +127,7 @@ __device__ __forceinline__ void rope_cs_fast(float hi, float lo, int pos, float 
 }
 
 template <bool kRope>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 4)
     decode_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
                        const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
                        const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
@@ -199,18 +214,24 @@ __global__ void __launch_bounds__(kWarps * 32)
           qv[hh][ks * 4 + e] = (x1 * cs[d] - x2 * sn[d]) * qs;
           qv[hh][(ks + 2) * 4 + e] = (x1 * sn[d] + x2 * cs[d]) * qs;
         }
-    auto lo = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
+    // kRope: the score product runs in fp16 (the rotated keys are rounded
+    // to fp16), so the query parts are fp16 too
+    auto pk = [](float x, float y) { return kRope ? pack_f16(x, y) : pack_bf16(x, y); };
+    auto lo = [](float x) {
+      return kRope ? x - __half2float(__float2half_rn(x))
+                   : x - __bfloat162float(__float2bfloat16_rn(x));
+    };
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
-      qa[ks][0] = pack_bf16(a0[0], a0[1]);
-      qa[ks][1] = pack_bf16(a1[0], a1[1]);
-      qa[ks][2] = pack_bf16(a0[2], a0[3]);
-      qa[ks][3] = pack_bf16(a1[2], a1[3]);
-      ql[ks][0] = pack_bf16(lo(a0[0]), lo(a0[1]));
-      ql[ks][1] = pack_bf16(lo(a1[0]), lo(a1[1]));
-      ql[ks][2] = pack_bf16(lo(a0[2]), lo(a0[3]));
-      ql[ks][3] = pack_bf16(lo(a1[2]), lo(a1[3]));
+      qa[ks][0] = pk(a0[0], a0[1]);
+      qa[ks][1] = pk(a1[0], a1[1]);
+      qa[ks][2] = pk(a0[2], a0[3]);
+      qa[ks][3] = pk(a1[2], a1[3]);
+      ql[ks][0] = pk(lo(a0[0]), lo(a0[1]));
+      ql[ks][1] = pk(lo(a1[0]), lo(a1[1]));
+      ql[ks][2] = pk(lo(a0[2]), lo(a0[3]));
+      ql[ks][3] = pk(lo(a1[2]), lo(a1[3]));
     }
   }
 
@@ -223,14 +244,18 @@ __global__ void __launch_bounds__(kWarps * 32)
   const uint32_t wsm_u = smem_u32(wsm);
   const int n_tiles = c0 < c1 ? (c1 - c0 + kTileKeys - 1) / kTileKeys : 0;
   // tiles of this warp: warp, warp + kWarps, ...
-  auto issue = [&](int it) {
+  // pool slot of key `lane` of this warp's tile it (0 past the end); loaded
+  // one tile ahead of its use, so the gather never waits on the index load
+  auto load_slot = [&](int it) {
+    const int k = c0 + (warp + it * kWarps) * kTileKeys + lane;
+    return lane < kTileKeys && k < c1 ? __ldg(indices + beg + k) : 0;
+  };
+  auto issue = [&](int it, int slot) {
     const int tile = warp + it * kWarps;
     const int stage = it % kStages;
     if (tile < n_tiles) {
       const int k0 = c0 + tile * kTileKeys;
-      int slot = 0;
       const bool have = lane < kTileKeys && k0 + lane < c1;
-      if (have) slot = __ldg(indices + beg + k0 + lane);
       if (kRope && lane < kTileKeys)  // the tile's positions (0 past the end)
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(
                          wsm_u + stage * kSB + 4096 + 4 * lane),
@@ -250,10 +275,17 @@ __global__ void __launch_bounds__(kWarps * 32)
   };
 
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+  int slot_nx = load_slot(0);
 #pragma unroll
-  for (int it = 0; it < kStages - 1; ++it) issue(it);
+  for (int it = 0; it < kStages - 1; ++it) {
+    const int sl = slot_nx;
+    slot_nx = load_slot(it + 1);
+    issue(it, sl);
+  }
   for (int it = 0; it < my_tiles; ++it) {
-    issue(it + kStages - 1);
+    const int sl = slot_nx;
+    slot_nx = load_slot(it + kStages);
+    issue(it + kStages - 1, sl);
     asm volatile("cp.async.wait_group %0;\n" ::"n"(kStages - 1));
     __syncwarp();
     const uint32_t kt = wsm_u + (it % kStages) * kSB, vt = kt + 2048;
@@ -262,7 +294,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (kRope) {
       const int32_t *tpos = reinterpret_cast<const int32_t *>(wsm + (it % kStages) * kSB + 4096);
       const int pa = tpos[gid], pb = tpos[gid + 8];
-      uint32_t kb[4][4], kl[4][4];
+      uint32_t kb[4][4];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const int mi = lane >> 3;
@@ -290,21 +322,15 @@ __global__ void __launch_bounds__(kWarps * 32)
           const float x2a = __low2float(bq), x2b = __high2float(bq);
           const float y1a = x1a * c0f - x2a * s0f, y1b = x1b * c1f - x2b * s1f;
           const float y2a = x1a * s0f + x2a * c0f, y2b = x1b * s1f + x2b * c1f;
-          kb[ks][r] = pack_bf16(y1a, y1b);
-          kb[ks + 2][r] = pack_bf16(y2a, y2b);
-          const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
-          const __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
-          kl[ks][r] = pack_bf16(y1a - __low2float(h1), y1b - __high2float(h1));
-          kl[ks + 2][r] = pack_bf16(y2a - __low2float(h2), y2b - __high2float(h2));
+          kb[ks][r] = pack_f16(y1a, y1b);
+          kb[ks + 2][r] = pack_f16(y2a, y2b);
         }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
-        mma_bf16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
-        mma_bf16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
-        mma_bf16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
-        mma_bf16(s[0], qa[ks], kl[ks][0], kl[ks][1]);
-        mma_bf16(s[1], qa[ks], kl[ks][2], kl[ks][3]);
+        mma_f16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+        mma_f16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+        mma_f16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+        mma_f16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
       }
     }
     // S = Q K^T: two n-blocks of 8 keys
