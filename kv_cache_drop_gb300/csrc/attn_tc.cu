@@ -442,12 +442,9 @@ cudaError_t launch_attn_tc_bf16(const PlanDev &p, void *out, cudaStream_t s) {
       !make_map(&mv, p.vp, (int64_t)p.Hkv * p.T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return cudaErrorInvalidValue;
   const int smem = (int)sizeof(Smem) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // per device, so set on every launch (cheap)
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   const int n_pairs = p.Hq / 2;
   const int64_t grid = (int64_t)p.n_qtiles * n_pairs;
   attn_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(mk, mv, p, (__nv_bfloat16 *)out,

@@ -736,12 +736,10 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         const int32_t *kvpos = nullptr) {
   // chunk: the largest of 4096, 2048, 1024 keys that still gives about two
   // waves of CTAs (4 per SM) when every request is max_kv long
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
-  }
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
   int chunk = kMaxChunk;
   while (chunk > kMinChunk && (int64_t)B * n_splits(max_kv, chunk) * Hkv < 2LL * 4 * sms) chunk /= 2;
   while (n_splits(max_kv, chunk) > kMaxSplits) chunk *= 2;

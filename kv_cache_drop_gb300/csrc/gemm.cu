@@ -180,12 +180,9 @@ cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void 
   CUtensorMap ma, mb;
   if (!make_map(&ma, x, M, K, BM) || !make_map(&mb, w, N, K, BN)) return cudaErrorInvalidValue;
   const int smem = (int)sizeof(GemmSmem) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // per device, so set on every launch (cheap)
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
   gemm_kernel<<<grid, kThreads, smem, s>>>(ma, mb, M, N, K, y, out_mode, status);
   return cudaGetLastError();
