@@ -29,6 +29,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "akv_internal.h"
 
 using namespace akv;
@@ -61,6 +63,18 @@ akv_status injected_fault(const char *entry) {
   if (!strcmp(f, "workspace")) return fail(AKV_ERR_WORKSPACE, "%s: injected fault", entry);
   return AKV_OK;
 }
+
+// Every entry point opens an NVTX range named after it (visible to nsys and
+// to ncu --nvtx; no cost without a tool attached), then applies AKV_FAULT.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define AKV_ENTRY(name)            \
+  NvtxRange akv_nvtx_range_(name); \
+  if (akv_status akv_fault_ = injected_fault(name)) return akv_fault_
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -595,7 +609,7 @@ akv_status plan_create_impl(const akv_shape *shape, int32_t n_req, const int32_t
                             const int32_t *logical_idx, const akv_oplog *ops,
                             const int32_t *share_from, const int32_t *share_len,
                             akv_plan **plan_out) {
-  if (akv_status f = injected_fault("akv_plan_create")) return f;
+  AKV_ENTRY("akv_plan_create");
   if (!plan_out) return fail(AKV_ERR_INVALID, "plan_out is NULL");
   *plan_out = nullptr;
   if (akv_status st = check_shape(shape)) return st;
@@ -726,7 +740,7 @@ akv_status check_run(const akv_plan *P, void *workspace, size_t workspace_bytes)
 
 akv_status akv_segment_prepare(const akv_plan *P, const void *q, const void *k, const void *v,
                                void *workspace, size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_segment_prepare")) return f;
+  AKV_ENTRY("akv_segment_prepare");
   if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
   if (P->T == 0) return AKV_OK;
   if (!q || !k || !v) return fail(AKV_ERR_INVALID, "NULL tensor");
@@ -744,7 +758,7 @@ akv_status akv_segment_prepare(const akv_plan *P, const void *q, const void *k, 
 
 akv_status akv_segment_attend(const akv_plan *P, void *out, void *workspace,
                               size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_segment_attend")) return f;
+  AKV_ENTRY("akv_segment_attend");
   if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
   if (P->T == 0) return AKV_OK;
   if (!out) return fail(AKV_ERR_INVALID, "NULL output");
@@ -760,7 +774,7 @@ akv_status akv_segment_attend(const akv_plan *P, void *out, void *workspace,
 akv_status akv_segment_attention_run(const akv_plan *P, const void *q, const void *k,
                                      const void *v, void *out, void *workspace,
                                      size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_segment_attention_run")) return f;
+  AKV_ENTRY("akv_segment_attention_run");
   if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
   if (P->T == 0) return AKV_OK;
   if (!q || !k || !v || !out) return fail(AKV_ERR_INVALID, "NULL tensor");
@@ -882,7 +896,7 @@ size_t akv_compact_workspace(const akv_oplog *ops, int32_t T) {
 akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *active_idx,
                        int32_t *active_pos, int32_t *n_active, void *workspace,
                        size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_compact")) return f;
+  AKV_ENTRY("akv_compact");
   if (akv_status st = check_oplog(ops, T, 0)) return st;
   if (!n_active || !active_idx || !active_pos) return fail(AKV_ERR_INVALID, "NULL output");
   CompactHost c;
@@ -952,7 +966,7 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
                               int32_t upto, const void *k_in, const void *v_in, void *k_out,
                               void *v_out, int32_t *n_out, void *workspace,
                               size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_repos_boundary")) return f;
+  AKV_ENTRY("akv_repos_boundary");
   if (akv_status st = check_shape(shape)) return st;
   if (akv_status st = check_oplog(ops, T, 0)) return st;
   if (!n_out) return fail(AKV_ERR_INVALID, "n_out is NULL");
@@ -993,7 +1007,7 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
 akv_status akv_repos_rotate(const akv_shape *shape, int32_t r, const int32_t *src_idx,
                             const int32_t *pos_from, const int32_t *pos_to, const void *k_in,
                             const void *v_in, void *k_out, void *v_out, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_repos_rotate")) return f;
+  AKV_ENTRY("akv_repos_rotate");
   if (akv_status st = check_shape(shape)) return st;
   if (r < 0) return fail(AKV_ERR_INVALID, "r < 0");
   if (r == 0) return AKV_OK;
@@ -1010,7 +1024,7 @@ akv_status akv_repos_rotate(const akv_shape *shape, int32_t r, const int32_t *sr
 akv_status akv_append_kv(const akv_shape *shape, int32_t n, const void *k_new, const void *v_new,
                          const int32_t *pos, const int32_t *slot, void *k_pool, void *v_pool,
                          akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_append_kv")) return f;
+  AKV_ENTRY("akv_append_kv");
   if (akv_status st = check_shape(shape)) return st;
   if (n < 0) return fail(AKV_ERR_INVALID, "n < 0");
   if (n == 0) return AKV_OK;
@@ -1034,7 +1048,7 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
                                 const int32_t *kv_indptr, const int32_t *kv_indices,
                                 int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
                                 akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_decode_attention")) return f;
+  AKV_ENTRY("akv_decode_attention");
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
   if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
@@ -1064,7 +1078,7 @@ akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const 
                                        const int32_t *kv_indices, int32_t max_kv, void *out,
                                        void *workspace, size_t workspace_bytes,
                                        akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_decode_attention_append")) return f;
+  AKV_ENTRY("akv_decode_attention_append");
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
   if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
@@ -1100,7 +1114,7 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
                                      const int32_t *kv_pos, int32_t max_kv, void *out,
                                      void *workspace, size_t workspace_bytes,
                                      akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_decode_attention_rope")) return f;
+  AKV_ENTRY("akv_decode_attention_rope");
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
   if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
@@ -1131,7 +1145,7 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
                                        const void *v_pool, const int32_t *kv_indptr,
                                        const int32_t *kv_indices, int32_t max_kv, void *out,
                                        akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_decode_attention_static")) return f;
+  AKV_ENTRY("akv_decode_attention_static");
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
   if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
@@ -1166,7 +1180,7 @@ size_t akv_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
 akv_status akv_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *x, const void *w, void *y,
                          int32_t out_mode, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_gemm_bf16")) return f;
+  AKV_ENTRY("akv_gemm_bf16");
   if (M < 0 || N < 0 || K <= 0 || out_mode < 0 || out_mode > 2)
     return fail(AKV_ERR_INVALID, "bad GEMM arguments");
   if (N % 32 || K % 8)
@@ -1183,7 +1197,7 @@ akv_status akv_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *x, const v
 
 akv_status akv_rmsnorm(int32_t rows, int32_t d, float eps, akv_dtype in_dtype, const void *x,
                        const float *weight, akv_dtype out_dtype, void *y, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_rmsnorm")) return f;
+  AKV_ENTRY("akv_rmsnorm");
   if (rows < 0 || d <= 0 || !(eps >= 0.f)) return fail(AKV_ERR_INVALID, "bad rmsnorm arguments");
   if (rows == 0) return AKV_OK;
   if (!x || !y) return fail(AKV_ERR_INVALID, "NULL argument");
@@ -1194,7 +1208,7 @@ akv_status akv_rmsnorm(int32_t rows, int32_t d, float eps, akv_dtype in_dtype, c
 }
 
 akv_status akv_swiglu(int64_t n, const void *g, const void *u, void *out, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_swiglu")) return f;
+  AKV_ENTRY("akv_swiglu");
   if (n < 0) return fail(AKV_ERR_INVALID, "n < 0");
   if (n == 0) return AKV_OK;
   if (!g || !u || !out) return fail(AKV_ERR_INVALID, "NULL argument");
@@ -1239,7 +1253,7 @@ size_t akv_decoder_workspace(const akv_plan *P, int32_t d_model, int32_t d_ff) {
 akv_status akv_decoder_forward(const akv_plan *P, int32_t n_layers, const akv_layer_weights *layers,
                                int32_t d_model, int32_t d_ff, float eps, const void *x, float *out,
                                void *workspace, size_t workspace_bytes, akv_stream_t stream) {
-  if (akv_status f = injected_fault("akv_decoder_forward")) return f;
+  AKV_ENTRY("akv_decoder_forward");
   if (!P || n_layers < 0 || (n_layers > 0 && !layers) || d_model <= 0 || d_ff <= 0 || !x || !out)
     return fail(AKV_ERR_INVALID, "bad decoder arguments");
   if (P->shape.dtype != AKV_BF16) return fail(AKV_ERR_UNSUPPORTED, "decoder layers run in bf16");
