@@ -59,9 +59,10 @@ constexpr float kE0 = 0.99992806f, kE1 = 0.69326097f, kE2 = 0.24261113f, kE3 = 0
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + it holds rint(x) in its low bits
 // hardware named barriers (0 is __syncthreads)
 // Named barrier kBarP + i, one generation per window n (plus one for the
-// prologue): softmax group i arrives once P_i(n) is in TMEM (128 threads),
+// prologue): softmax group i syncs once P_i(n) is in TMEM (128 threads),
 // the TMA producer syncs once window n+1 has landed (32), and the MMA warp
-// syncs before issuing P_i.V(n) and S_i(n+1) (32).
+// syncs before issuing P_i.V(n) and S_i(n+1) (32).  Every role waits for
+// each generation to complete, so the counts of two generations never mix.
 constexpr int kBarP = 3;
 constexpr int kBarPCount = 192;
 
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st32(tmem + lane_base + 416 + 32 * i, qw);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::named_bar_arrive(kBarP + i, kBarPCount);
+      ptx::named_bar_sync(kBarP + i, kBarPCount);
     }
     const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
     float m_run = -INFINITY;
@@ -367,7 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::named_bar_arrive(kBarP + i, kBarPCount);  // P_i (and a rescaled O_i) are in TMEM
+      // P_i (and a rescaled O_i) are in TMEM.  The softmax waits for the
+      // generation to complete (its next S_i is issued after it anyway), so
+      // no role can reach a later generation of this barrier before the
+      // current one has all its arrivals, even after a timed-out wait
+      ptx::named_bar_sync(kBarP + i, kBarPCount);
     }
     wait_bar(&sm.bar_o[i], (n_win - 1) & 1, p.status);
     ptx::tc_fence_after();
