@@ -17,6 +17,7 @@
 // fp32: one thread per key, FMA dot products, block-level merge.
 #include "common.cuh"
 
+#include <algorithm>
 #include <mutex>
 
 namespace akv {
@@ -747,7 +748,9 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
   Partials part = partials(ws, B, Hq, max_kv, chunk);
   int *counters = reinterpret_cast<int *>(static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv));
   const bool rope = kvpos != nullptr;
-  const int smem = kWarps * kStages * kStageBytes(rope);
+  // dynamic shared memory: the tile buffers, or the merge's per-split
+  // weights ([16 rows][ns] floats and 16 row totals) when those are larger
+  const int smem = std::max(kWarps * kStages * kStageBytes(rope), (16 * ns + 16) * 4);
   auto kern = rope ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -249,6 +249,16 @@ def test_decode_peaky_and_empty_request():
     assert float(out.abs().max()) == 0.0
 
 
+def test_decode_many_splits():
+    """One request of 1.5M keys on a single KV head with 16 query heads: few
+    CTAs, so the key chunk shrinks and the request is cut into ~730 splits,
+    whose merge weights need more shared memory than the tile buffers."""
+    dw = workloads.decode_workload(seed=15, B=1, active=(1_500_000, 1_500_000), steps=1,
+                                   Hq=16, Hkv=1)
+    res = _run_decode(dw, {0})
+    assert_close(res[0], _decode_oracle(dw, 0, oracle.widen(dw.q[0], "bf16")), "bf16")
+
+
 def test_decode_full_size_steps():
     """14 requests, 20k-90k active keys each, 256 decode steps with appends;
     steps 0, 1 and 255 checked in full."""
