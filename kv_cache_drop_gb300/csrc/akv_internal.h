@@ -110,6 +110,12 @@ cudaError_t launch_repos_boundary(int dtype, int Hkv, int r, int nk, const int32
                                   const int32_t *kprefix, const int32_t *kpos, const void *kin,
                                   const void *vin, void *kout, void *vout, const RopeTheta &th,
                                   cudaStream_t s);
+// the same with the run tables in the kernel's parameters (nk <= repos_inline_runs())
+int repos_inline_runs();
+cudaError_t launch_repos_boundary_inline(int dtype, int Hkv, int r, int nk, const int32_t *kstart,
+                                         const int32_t *kprefix, const int32_t *kpos,
+                                         const void *kin, const void *vin, void *kout, void *vout,
+                                         const RopeTheta &th, cudaStream_t s);
 
 struct CompactDev {
   const int32_t *msg_start;  // [n_msgs+1]
@@ -125,6 +131,23 @@ struct CompactDev {
 cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *active_pos,
                            cudaStream_t s);
 int compact_blocks(int T);
+
+// Small host tables delivered as the parameters of a copy kernel on the
+// stream: a launch costs far less latency than starting the copy engine for
+// a few hundred bytes.  Segment s copies seg[s].bytes bytes from
+// data + seg[s].src_off to dst + seg[s].dst_off.
+constexpr int kParamBlobBytes = 3840;
+constexpr int kParamMaxSegs = 8;
+struct ParamSeg {
+  uint32_t dst_off, src_off, bytes;
+};
+struct ParamBlob {
+  int32_t n_seg;
+  ParamSeg seg[kParamMaxSegs];
+  alignas(16) uint8_t data[kParamBlobBytes];
+};
+static_assert(sizeof(ParamBlob) + sizeof(void *) <= 4096, "kernel parameter space");
+cudaError_t launch_param_upload(char *dst, const ParamBlob &blob, cudaStream_t s);
 
 size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope = false);
 // partials + the per-(request, KV head) merge counters of the bf16 kernel

@@ -474,11 +474,25 @@ PinnedPool &pinned_pool() {
 }
 
 // Copies the parts to dst + dst_off on stream s without waiting for the
-// stream.  Falls back to plain (blocking) copies when no pinned memory can
-// be had.
+// stream.  A few KB at most travel as the parameters of a copy kernel (no
+// copy-engine start-up); larger uploads go through the pinned blocks, or
+// plain (blocking) copies when no pinned memory can be had.
 cudaError_t upload_async(char *dst, const HostPart *parts, int n, cudaStream_t s) {
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align_up(parts[i].bytes, 16);
+  if (total <= (size_t)kParamBlobBytes && n <= kParamMaxSegs) {
+    ParamBlob blob;
+    blob.n_seg = 0;
+    size_t o = 0;
+    for (int i = 0; i < n; ++i) {
+      if (!parts[i].bytes) continue;
+      std::memcpy(blob.data + o, parts[i].src, parts[i].bytes);
+      blob.seg[blob.n_seg++] = ParamSeg{(uint32_t)parts[i].dst_off, (uint32_t)o,
+                                        (uint32_t)parts[i].bytes};
+      o += align_up(parts[i].bytes, 16);
+    }
+    return launch_param_upload(dst, blob, s);
+  }
   PinnedPool::Block blk;
   if (!pinned_pool().acquire(total, &blk)) {
     for (int i = 0; i < n; ++i) {
@@ -981,6 +995,15 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
   std::vector<int32_t> kstart, kprefix, kpos;
   kept_runs(ops, c, &kstart, &kprefix, &kpos);
   const int nk = (int)kstart.size();
+  if (nk >= 1 && nk <= repos_inline_runs()) {  // the tables travel with the launch
+    RopeTheta th;
+    rope_theta(shape->rope_base, &th);
+    cudaError_t e = launch_repos_boundary_inline(shape->dtype, shape->Hkv, (int)c.n_active, nk,
+                                                 kstart.data(), kprefix.data(), kpos.data(), k_in,
+                                                 v_in, k_out, v_out, th, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "repos at boundary");
+    return AKV_OK;
+  }
   // one upload: [kstart | kprefix | kpos]
   std::vector<int32_t> packed;
   packed.reserve(3 * nk + 1);

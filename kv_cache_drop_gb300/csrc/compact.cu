@@ -122,9 +122,22 @@ __global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev c, i
   }
 }
 
+__global__ void __launch_bounds__(256) param_upload_kernel(const ParamBlob blob, char *dst) {
+  for (int sg = 0; sg < blob.n_seg; ++sg) {
+    const ParamSeg g = blob.seg[sg];
+    for (uint32_t i = threadIdx.x; i < g.bytes; i += blockDim.x)
+      dst[g.dst_off + i] = (char)blob.data[g.src_off + i];
+  }
+}
+
 }  // namespace
 
 int compact_blocks(int T) { return (T + kBlock - 1) / kBlock; }
+
+cudaError_t launch_param_upload(char *dst, const ParamBlob &blob, cudaStream_t s) {
+  param_upload_kernel<<<1, 256, 0, s>>>(blob, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *active_pos,
                            cudaStream_t s) {

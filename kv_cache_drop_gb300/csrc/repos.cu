@@ -107,9 +107,29 @@ struct KeptRuns {
   }
 };
 
+// rows of akv_repos_boundary with the run tables carried in the kernel's
+// parameters (no upload), for up to kInlineRuns runs: kstart[nk] |
+// kprefix[nk + 1] | kpos[nk]
+constexpr int kInlineRuns = 256;
+struct KeptRunsInline {
+  int nk;
+  int32_t t[3 * kInlineRuns + 1];
+  __device__ __forceinline__ void get(int j, int64_t *in, int32_t *delta) const {
+    const int32_t *kstart = t, *kprefix = t + nk, *kpos = t + 2 * nk + 1;
+    int lo = 0, hi = nk;  // kprefix[lo] <= j < kprefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (kprefix[mid] <= j) lo = mid; else hi = mid;
+    }
+    const int off = j - kprefix[lo];
+    *in = kstart[lo] + off;
+    *delta = j - (kpos[lo] + off);
+  }
+};
+
 template <typename T, typename Rows>
 __global__ void __launch_bounds__(kThreads)
-    repos_stream_kernel(int Hkv, int n, Rows rs, const T *__restrict__ kin,
+    repos_stream_kernel(int Hkv, int n, const __grid_constant__ Rows rs, const T *__restrict__ kin,
                         const T *__restrict__ vin, T *__restrict__ kout, T *__restrict__ vout,
                         RopeTheta th) {
   constexpr int E = Chunk<T>::kElems;
@@ -213,6 +233,24 @@ cudaError_t launch_repos_boundary(int dtype, int Hkv, int r, int nk, const int32
                                   const void *vin, void *kout, void *vout, const RopeTheta &th,
                                   cudaStream_t s) {
   const KeptRuns rs{nk, kstart, kprefix, kpos};
+  if (dtype == AKV_F32) return repos_stream<float>(Hkv, r, rs, kin, vin, kout, vout, th, s);
+  return repos_stream<__nv_bfloat16>(Hkv, r, rs, kin, vin, kout, vout, th, s);
+}
+
+int repos_inline_runs() { return kInlineRuns; }
+
+cudaError_t launch_repos_boundary_inline(int dtype, int Hkv, int r, int nk, const int32_t *kstart,
+                                         const int32_t *kprefix, const int32_t *kpos,
+                                         const void *kin, const void *vin, void *kout, void *vout,
+                                         const RopeTheta &th, cudaStream_t s) {
+  if (nk < 1 || nk > kInlineRuns) return cudaErrorInvalidValue;
+  KeptRunsInline rs;
+  rs.nk = nk;
+  for (int i = 0; i < nk; ++i) {
+    rs.t[i] = kstart[i];
+    rs.t[2 * nk + 1 + i] = kpos[i];
+  }
+  for (int i = 0; i <= nk; ++i) rs.t[nk + i] = kprefix[i];
   if (dtype == AKV_F32) return repos_stream<float>(Hkv, r, rs, kin, vin, kout, vout, th, s);
   return repos_stream<__nv_bfloat16>(Hkv, r, rs, kin, vin, kout, vout, th, s);
 }

@@ -117,6 +117,27 @@ def test_repos_boundary_every_boundary(seed, dtype):
             assert np.array_equal(gv, rv)
 
 
+@pytest.mark.parametrize("n", [600, 700])
+def test_repos_boundary_many_runs(n):
+    """n short messages, every other one dropped at the last boundary: n/2
+    separate kept runs, more than the repos kernel's parameters carry, so the
+    run tables are uploaded (600: as a copy kernel's parameters, 700: through
+    pinned host memory); compaction's tables take the same two paths."""
+    lens = np.random.default_rng(5).integers(1, 5, size=n)
+    ms = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    drops = [(n - 1, j) for j in range(1, n, 2)]
+    r = workloads.gen._trajectory("runs", 97, ms, ["m"] * n, drops, [], 4, 2, 64, "bf16")
+    gk, gv = _repos_boundary(r, n - 1, "bf16", akv.shape(4, 2, 64, "bf16"))
+    ou, op = oracle.compact(*r.ops(), upto=n - 1)
+    rk, rv = oracle.repos_rotate(r.k, r.v, ou, op, np.arange(len(ou)), "bf16", 10000.0)
+    assert gk.shape == rk.shape and len(ou) > 0
+    assert np.max(np.abs(gk - rk)) <= 2 ** -8 * 4
+    assert np.array_equal(gv, rv)
+    gi, gp = _compact(r.ops(), r.T, n - 1)
+    np.testing.assert_array_equal(gi, ou)
+    np.testing.assert_array_equal(gp, op)
+
+
 def test_repos_boundary_full_size():
     """128k trajectory, one-pass repos at its repos boundary."""
     r = workloads.repos_config()
