@@ -13,17 +13,38 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kPer = 8;  // consecutive tokens per thread
+constexpr int kThreads = 256;
+constexpr int kPer = 4;  // consecutive tokens per thread
 constexpr int kBlock = kThreads * kPer;
+
+constexpr int kSmemMsgs = 2048;  // per-message tables staged in shared memory up to this size
 
 __device__ __forceinline__ int msg_of(const int32_t *ms, int n_msgs, int u) {
   int lo = 0, hi = n_msgs;  // ms[lo] <= u < ms[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(ms + mid) <= u) lo = mid; else hi = mid;
+    if (ms[mid] <= u) lo = mid; else hi = mid;
   }
   return lo;
+}
+
+// The message of a token is found by binary search in msg_start, a chain of
+// dependent loads: the block first copies the per-message tables into
+// shared memory (coalesced) and searches there.  Returns the view to use.
+__device__ __forceinline__ CompactDev stage_tables(const CompactDev &c, int32_t *s_ms,
+                                                   uint8_t *s_keep, uint8_t *s_alive) {
+  if (c.n_msgs > kSmemMsgs) return c;
+  for (int i = threadIdx.x; i <= c.n_msgs; i += blockDim.x) s_ms[i] = __ldg(c.msg_start + i);
+  for (int i = threadIdx.x; i < c.n_msgs; i += blockDim.x) {
+    s_keep[i] = __ldg(c.keep + i);
+    s_alive[i] = __ldg(c.alive_br + i);
+  }
+  __syncthreads();
+  CompactDev v = c;
+  v.msg_start = s_ms;
+  v.keep = s_keep;
+  v.alive_br = s_alive;
+  return v;
 }
 
 // flags of the kPer tokens of this thread: bit i of keep / alive
@@ -36,7 +57,7 @@ __device__ __forceinline__ void token_flags(const CompactDev &c, int u0, uint32_
   for (int i = 0; i < kPer; ++i) {
     const int u = u0 + i;
     if (u >= c.T) break;
-    while (__ldg(c.msg_start + m + 1) <= u) ++m;
+    while (c.msg_start[m + 1] <= u) ++m;
     if (c.keep[m]) *keep |= 1u << i;
     if (c.has_br && u < c.br_end && c.alive_br[m]) *alive |= 1u << i;
   }
@@ -69,7 +90,10 @@ __device__ __forceinline__ uint32_t block_exscan(uint32_t x, uint32_t *total) {
   return before;
 }
 
-__global__ void __launch_bounds__(kThreads) compact_count_kernel(CompactDev c) {
+__global__ void __launch_bounds__(kThreads) compact_count_kernel(CompactDev cg) {
+  __shared__ int32_t s_ms[kSmemMsgs + 1];
+  __shared__ uint8_t s_keep[kSmemMsgs], s_alive[kSmemMsgs];
+  const CompactDev c = stage_tables(cg, s_ms, s_keep, s_alive);
   uint32_t keep, alive;
   token_flags(c, blockIdx.x * kBlock + threadIdx.x * kPer, &keep, &alive);
   uint32_t total;
@@ -80,8 +104,11 @@ __global__ void __launch_bounds__(kThreads) compact_count_kernel(CompactDev c) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev c, int32_t *active_idx,
+__global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev cg, int32_t *active_idx,
                                                                  int32_t *active_pos) {
+  __shared__ int32_t s_ms[kSmemMsgs + 1];
+  __shared__ uint8_t s_keep[kSmemMsgs], s_alive[kSmemMsgs];
+  const CompactDev c = stage_tables(cg, s_ms, s_keep, s_alive);
   __shared__ int32_t base_keep, base_alive;
   if (threadIdx.x < 32) {
     int32_t a = 0, b = 0;
