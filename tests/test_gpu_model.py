@@ -65,6 +65,14 @@ def test_rmsnorm_and_swiglu():
     gg, uu = oracle.widen(g, "bf16"), oracle.widen(u, "bf16")
     sref = gg / (1 + np.exp(-gg)) * uu
     assert np.max(np.abs(out.float().cpu().numpy() - sref) / (np.abs(sref) + 1e-3)) <= 2 ** -7
+    # a ragged tail (4,999 = 624 groups of 8 + 7) and pointers one element off
+    # 16-byte alignment (the element-wise path): the same values bit for bit
+    gd, ud = _bf16(g), _bf16(u)
+    for off, n in ((0, 4999), (1, 4998)):
+        o2 = torch.zeros(5000, dtype=torch.bfloat16, device="cuda")
+        akv.akv_swiglu(n, gd[off:off + n], ud[off:off + n], o2[off:off + n])
+        torch.cuda.synchronize()
+        assert torch.equal(o2[off:off + n], out[off:off + n]), (off, n)
 
 
 def _gpu_weights(mw):
