@@ -174,6 +174,10 @@ cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void 
 cudaError_t launch_rmsnorm(int rows, int d, float eps, int in_f32, const void *x, const float *w,
                            int out_f32, void *y, cudaStream_t s);
 cudaError_t launch_swiglu(int64_t n, const void *g, const void *u, void *out, cudaStream_t s);
+// gate [d_ff][K] and up [d_ff][K] into [2 d_ff][K] with 128-row blocks
+// alternating, for the SwiGLU GEMM (out_mode 3); d_ff % 128 == 0, K % 8 == 0
+cudaError_t launch_interleave_gu(const void *wg, const void *wu, void *wgu, int d_ff, int K,
+                                 cudaStream_t s);
 cudaError_t launch_widen(int64_t n, const void *x, float *y, cudaStream_t s);
 
 // Decode with its split-KV partials in a static device array (no workspace).

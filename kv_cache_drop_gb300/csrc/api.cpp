@@ -1242,7 +1242,7 @@ akv_status akv_swiglu(int64_t n, const void *g, const void *u, void *out, akv_st
 
 namespace {
 struct DecoderLayout {
-  size_t h, a, q, k, v, o, g, u, attn, total;
+  size_t h, a, q, k, v, o, g, u, wgu, attn, total;
 };
 DecoderLayout decoder_layout(const akv_plan *P, int d_model, int d_ff) {
   DecoderLayout L{};
@@ -1262,7 +1262,11 @@ DecoderLayout decoder_layout(const akv_plan *P, int d_model, int d_ff) {
   L.v = take(2 * T * P->shape.Hkv * kD);
   L.o = take(2 * T * P->shape.Hq * kD);
   L.g = take(2 * T * d_ff);
-  L.u = take(2 * T * d_ff);
+  // d_ff a multiple of 128: gate and up run as one GEMM with a SwiGLU
+  // epilogue over interleaved weights ([2 d_ff][d_model]); otherwise as two
+  // GEMMs into g and u, then SwiGLU
+  if (d_ff % 128 == 0) L.wgu = take(2 * 2 * (size_t)d_ff * d_model);
+  else L.u = take(2 * T * d_ff);
   L.total = align_up(off, 1024);
   return L;
 }
@@ -1295,7 +1299,8 @@ akv_status akv_decoder_forward(const akv_plan *P, int32_t n_layers, const akv_la
   char *b = (char *)workspace;
   float *h = (float *)(b + L.h);
   void *a = b + L.a, *q = b + L.q, *k = b + L.k, *v = b + L.v, *o = b + L.o, *g = b + L.g,
-       *u = b + L.u, *aws = b + L.attn;
+       *u = b + L.u, *wgu = b + L.wgu, *aws = b + L.attn;
+  const bool fused_ffn = d_ff % 128 == 0;
   const int T = (int)P->T, dq = P->shape.Hq * kD, dkv = P->shape.Hkv * kD;
   uint32_t *status = (uint32_t *)((char *)aws + P->ws.status);
   // The kernels' bounded waits stop waiting once this word is nonzero (a
@@ -1319,9 +1324,14 @@ akv_status akv_decoder_forward(const akv_plan *P, int32_t n_layers, const akv_la
       return st;
     AKV_TRY(launch_gemm(T, d_model, dq, o, w.wo, h, 2, status, s), "output projection");
     AKV_TRY(launch_rmsnorm(T, d_model, eps, 1, h, nullptr, 0, a, s), "rmsnorm");
-    AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wg, g, 0, status, s), "gate projection");
-    AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wu, u, 0, status, s), "up projection");
-    AKV_TRY(launch_swiglu((int64_t)T * d_ff, g, u, g, s), "swiglu");
+    if (fused_ffn) {  // gate and up as one GEMM, SwiGLU in its epilogue
+      AKV_TRY(launch_interleave_gu(w.wg, w.wu, wgu, d_ff, d_model, s), "gate/up interleave");
+      AKV_TRY(launch_gemm(T, 2 * d_ff, d_model, a, wgu, g, 3, status, s), "gate/up projection");
+    } else {
+      AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wg, g, 0, status, s), "gate projection");
+      AKV_TRY(launch_gemm(T, d_ff, d_model, a, w.wu, u, 0, status, s), "up projection");
+      AKV_TRY(launch_swiglu((int64_t)T * d_ff, g, u, g, s), "swiglu");
+    }
     AKV_TRY(launch_gemm(T, d_model, d_ff, g, w.wd, h, 2, status, s), "down projection");
   }
   AKV_TRY(launch_rmsnorm(T, d_model, eps, 1, h, nullptr, 1, out, s), "final rmsnorm");

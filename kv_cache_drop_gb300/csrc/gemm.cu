@@ -32,7 +32,10 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_
   ptx::mbar_wait_grid(bar, parity, status, kStatusWaitTimeout, kWaitBudget);
 }
 
-// out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add into Y
+// out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add into Y, 3 SwiGLU: W holds
+// gate and up rows interleaved in blocks of 128 (launch_interleave_gu), so a
+// tile's accumulator columns 0-127 are gate and 128-255 the matching up
+// columns; Y [M][N/2] bf16 gets silu(gate) * up
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int M, int N, int K, void *__restrict__ Y, int out_mode, uint32_t *status) {
@@ -94,8 +97,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_bar(&sm.done, 0, status);
     ptx::tc_fence_after();
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    if (out_mode == 3) {
+      const int NO = N / 2;  // output columns
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+        uint32_t gr[32], ur[32];
+        ptx::tmem_ld32(tl + c0, gr);
+        ptx::tmem_ld32(tl + BN / 2 + c0, ur);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence32(gr);
+        ptx::reg_fence32(ur);
+        const int n = n0 / 2 + c0;
+        if (m >= M || n >= NO) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * NO + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * q + 2 * e;
+            const float g0 = __uint_as_float(gr[c]), g1 = __uint_as_float(gr[c + 1]);
+            const float y0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(ur[c]);
+            const float y1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(ur[c + 1]);
+            __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+            w[e] = *reinterpret_cast<uint32_t *>(&h);
+          }
+          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN && out_mode != 3; c0 += 32) {
       uint32_t r[32];
       ptx::tmem_ld32(tl + c0, r);
       ptx::tmem_wait_ld();
@@ -138,6 +170,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, BN);
+  }
+}
+
+// wgu[256 j + c] = wg[128 j + c] (c < 128), wu[128 j + c - 128] (c >= 128):
+// rows of K bf16, copied 16 bytes at a time
+__global__ void interleave_gu_kernel(const uint4 *__restrict__ wg, const uint4 *__restrict__ wu,
+                                     uint4 *__restrict__ wgu, int d_ff, int k16) {
+  const int64_t total = (int64_t)2 * d_ff * k16;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / k16, c16 = i % k16;
+    const int64_t j = r / 256, c = r % 256;
+    const uint4 *src = c < 128 ? wg + (128 * j + c) * k16 : wu + (128 * j + c - 128) * k16;
+    wgu[i] = src[c16];
   }
 }
 
@@ -185,6 +231,15 @@ cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void 
   if (e != cudaSuccess) return e;
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
   gemm_kernel<<<grid, kThreads, smem, s>>>(ma, mb, M, N, K, y, out_mode, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_interleave_gu(const void *wg, const void *wu, void *wgu, int d_ff, int K,
+                                 cudaStream_t s) {
+  if ((d_ff % 128) || (K % 8)) return cudaErrorInvalidValue;
+  const int k16 = K / 8;
+  interleave_gu_kernel<<<1216, 256, 0, s>>>((const uint4 *)wg, (const uint4 *)wu, (uint4 *)wgu,
+                                            d_ff, k16);
   return cudaGetLastError();
 }
 

@@ -145,6 +145,19 @@ def _rel(got, ref):
     return float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(ref * ref))), float(np.abs(d).max())
 
 
+def test_decoder_ffn_two_gemms():
+    """d_ff = 1056, not a multiple of 128: gate and up run as two GEMMs and a
+    separate SwiGLU instead of one GEMM with a SwiGLU epilogue."""
+    mw = workloads.model_workload(seed=6, n_req=1, prefix=128, following=384, n_layers=2,
+                                  d_ff=1056, asst_len=(20, 60), tool_len=(60, 150))
+    got = run_decoder(mw)
+    ref = oracle.model_replay(mw.weights, mw.x, mw.msg_start, *mw.ops[0], mw.Hq, mw.Hkv, mw.D,
+                              mw.rope_base, mw.eps)
+    rel, mx = _rel(got, ref)
+    print(f"[parity] decoder d_ff=1056: rel_rms={rel:.3e} max_abs={mx:.3e}")
+    assert rel <= MODEL_REL_RMS and mx <= MODEL_MAX_ABS
+
+
 def test_decoder_small_vs_oracle():
     """Three requests, 4 layers at the full layer shape (d 1024, 16/4 heads,
     SwiGLU 4096), shared 128-token prefix + 640 diverging tokens."""
