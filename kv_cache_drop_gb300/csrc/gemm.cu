@@ -2,12 +2,14 @@
 // review page section 4.2, Appendix A.1.1: attention is segmented, the FFN
 // runs once over the whole sequence):  Y[M,N] (+)= X[M,K] * W[N,K]^T.
 //
-// tcgen05 GEMM, one CTA per 128 x 256 output tile: warp 0 streams 64-wide K
-// blocks of X and W with TMA (128-byte swizzle) through a 4-stage ring, warp 1
-// allocates 256 TMEM columns and issues 128x256x16 MMAs from one thread,
-// warps 2-5 (one TMEM lane quarter each) read the fp32 accumulator back and
-// write bf16, fp32, or add into an fp32 output (the residual stream).
-// Waits are bounded like the attention kernel's.
+// tcgen05 GEMM over 128 x 256 output tiles, persistent (one CTA per SM):
+// warp 0 streams 64-wide K blocks of X and W with TMA (128-byte swizzle)
+// through a 4-stage ring, warp 1 allocates two 256-column TMEM accumulators
+// and issues 128x256x16 MMAs from one thread, warps 2-5 (one TMEM lane
+// quarter each) read an accumulator back and write bf16, fp32, add into an
+// fp32 output (the residual stream) or apply SwiGLU, while the next tile
+// accumulates into the other one.  Waits are bounded like the attention
+// kernel's.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -24,7 +26,8 @@ constexpr long long kWaitBudget = 1000000000LL;
 struct __align__(1024) GemmSmem {
   uint8_t a[kStages][kABytes];
   uint8_t b[kStages][kBBytes];
-  uint64_t full[kStages], empty[kStages], done;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t acc_full[2], acc_empty[2];  // accumulator b: MMAs done / drained by the epilogue
   uint32_t tmem_base;
 };
 
@@ -32,10 +35,88 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_
   ptx::mbar_wait_grid(bar, parity, status, kStatusWaitTimeout, kWaitBudget);
 }
 
+// Epilogue of one 128 x 256 tile: this thread's row of the accumulator at
+// TMEM address tl (its lane, column 0) into Y.
 // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add into Y, 3 SwiGLU: W holds
 // gate and up rows interleaved in blocks of 128 (launch_interleave_gu), so a
 // tile's accumulator columns 0-127 are gate and 128-255 the matching up
 // columns; Y [M][N/2] bf16 gets silu(gate) * up
+__device__ __forceinline__ void store_tile(uint32_t tl, int m, int n0, int M, int N, void *Y,
+                                           int out_mode) {
+  if (out_mode == 3) {
+    const int NO = N / 2;  // output columns
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+      uint32_t gr[32], ur[32];
+      ptx::tmem_ld32(tl + c0, gr);
+      ptx::tmem_ld32(tl + BN / 2 + c0, ur);
+      ptx::tmem_wait_ld();
+      ptx::reg_fence32(gr);
+      ptx::reg_fence32(ur);
+      const int n = n0 / 2 + c0;
+      if (m >= M || n >= NO) continue;
+      uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * NO + n);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * q + 2 * e;
+          const float g0 = __uint_as_float(gr[c]), g1 = __uint_as_float(gr[c + 1]);
+          const float y0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(ur[c]);
+          const float y1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(ur[c + 1]);
+          __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+          w[e] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tl + c0, r);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence32(r);
+    const int n = n0 + c0;
+    if (m >= M || n >= N) continue;  // N is a multiple of 32
+    if (out_mode == 0) {
+      uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * N + n);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * e]),
+                                                   __uint_as_float(r[8 * q + 2 * e + 1]));
+          w[e] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(Y) + (int64_t)m * N + n);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        if (out_mode == 2) {
+          const float4 o = dst[q];
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        dst[q] = v;
+      }
+    }
+  }
+}
+
+// Persistent: CTA c takes output tiles c, c + gridDim.x, ... (row-major over
+// the tile grid, so consecutive tiles share their X rows).  The K-block ring
+// runs on across tiles; TMEM holds two 256-column accumulators, so the
+// epilogue warps drain tile j while the MMA thread computes tile j + 1.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int M, int N, int K, void *__restrict__ Y, int out_mode, uint32_t *status) {
@@ -43,17 +124,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   GemmSmem &sm = *reinterpret_cast<GemmSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int nk = (K + BK - 1) / BK;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = tiles_n * ((M + BM - 1) / BM);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
       ptx::mbar_init(&sm.empty[s], 1);
     }
-    ptx::mbar_init(&sm.done, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm.acc_full[b], 1);
+      ptx::mbar_init(&sm.acc_empty[b], 4);  // one arrival per epilogue warp
+    }
     ptx::fence_barrier_init();
   }
-  if (warp == 1) ptx::tmem_alloc(&sm.tmem_base, BN);
+  if (warp == 1) ptx::tmem_alloc(&sm.tmem_base, 2 * BN);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -63,113 +148,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmA);
       ptx::tma_prefetch_desc(&tmB);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages) wait_bar(&sm.empty[s], ((kb / kStages) - 1) & 1, status);
-        ptx::mbar_expect_tx(&sm.full[s], kABytes + kBBytes);
-        ptx::tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * BK, m0);
-        ptx::tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * BK, n0);
+      int c = 0;  // K blocks loaded so far, over all tiles
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++c) {
+          const int s = c % kStages;
+          if (c >= kStages) wait_bar(&sm.empty[s], ((c / kStages) - 1) & 1, status);
+          ptx::mbar_expect_tx(&sm.full[s], kABytes + kBBytes);
+          ptx::tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * BK, m0);
+          ptx::tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * BK, n0);
+        }
       }
-      for (int kb = nk > kStages ? nk - kStages : 0; kb < nk; ++kb)
-        wait_bar(&sm.full[kb % kStages], (kb / kStages) & 1, status);
+      // every copy has landed before the CTA exits
+      for (int c2 = c > kStages ? c - kStages : 0; c2 < c; ++c2)
+        wait_bar(&sm.full[c2 % kStages], (c2 / kStages) & 1, status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id = ptx::idesc_bf16(BM, BN, false);
       const uint64_t da = ptx::sdesc_sw128(ptx::smem_addr(sm.a[0]));
       const uint64_t db = ptx::sdesc_sw128(ptx::smem_addr(sm.b[0]));
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        wait_bar(&sm.full[s], (kb / kStages) & 1, status);
+      int c = 0;
+      int j = 0;  // this CTA's tile count
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+        const int acc = j & 1;
+        // accumulator acc was last used by tile j - 2: wait until drained
+        if (j >= 2) wait_bar(&sm.acc_empty[acc], ((j >> 1) - 1) & 1, status);
         ptx::tc_fence_after();
-        const uint64_t a0 = da + s * (kABytes >> 4), b0 = db + s * (kBBytes >> 4);
+        const uint32_t d = tmem + BN * acc;
+        for (int kb = 0; kb < nk; ++kb, ++c) {
+          const int s = c % kStages;
+          wait_bar(&sm.full[s], (c / kStages) & 1, status);
+          ptx::tc_fence_after();
+          const uint64_t a0 = da + s * (kABytes >> 4), b0 = db + s * (kBBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          ptx::mma_f16_ss(tmem, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(&sm.empty[s]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            ptx::mma_f16_ss(d, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(&sm.empty[s]);
+        }
+        ptx::mma_commit(&sm.acc_full[acc]);
       }
-      ptx::mma_commit(&sm.done);
     }
   } else {
     // epilogue: warp w owns TMEM lanes 32*(w%4) .. +31 = tile rows
     const int row = 32 * (warp & 3) + lane;
-    const int m = m0 + row;
-    wait_bar(&sm.done, 0, status);
-    ptx::tc_fence_after();
-    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    if (out_mode == 3) {
-      const int NO = N / 2;  // output columns
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-        uint32_t gr[32], ur[32];
-        ptx::tmem_ld32(tl + c0, gr);
-        ptx::tmem_ld32(tl + BN / 2 + c0, ur);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence32(gr);
-        ptx::reg_fence32(ur);
-        const int n = n0 / 2 + c0;
-        if (m >= M || n >= NO) continue;
-        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * NO + n);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * q + 2 * e;
-            const float g0 = __uint_as_float(gr[c]), g1 = __uint_as_float(gr[c + 1]);
-            const float y0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(ur[c]);
-            const float y1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(ur[c + 1]);
-            __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
-            w[e] = *reinterpret_cast<uint32_t *>(&h);
-          }
-          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-    }
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN && out_mode != 3; c0 += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tl + c0, r);
-      ptx::tmem_wait_ld();
-      ptx::reg_fence32(r);
-      const int n = n0 + c0;
-      if (m >= M || n >= N) continue;  // N is a multiple of 32
-      if (out_mode == 0) {
-        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(Y) + (int64_t)m * N + n);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * e]),
-                                                     __uint_as_float(r[8 * q + 2 * e + 1]));
-            w[e] = *reinterpret_cast<uint32_t *>(&h);
-          }
-          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      } else {
-        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(Y) + (int64_t)m * N + n);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-          if (out_mode == 2) {
-            const float4 o = dst[q];
-            v.x += o.x;
-            v.y += o.y;
-            v.z += o.z;
-            v.w += o.w;
-          }
-          dst[q] = v;
-        }
-      }
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    int j = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+      const int acc = j & 1;
+      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      wait_bar(&sm.acc_full[acc], (j >> 1) & 1, status);
+      ptx::tc_fence_after();
+      store_tile(tmem + lanes + BN * acc, m0 + row, n0, M, N, Y, out_mode);
+      // this warp's reads of the accumulator are complete (tmem_wait_ld in
+      // store_tile): hand it back to the MMA thread
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.acc_empty[acc]);
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, BN);
+    ptx::tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -229,7 +271,12 @@ cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void 
   // per device, so set on every launch (cheap)
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int64_t n_tiles = (int64_t)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
   gemm_kernel<<<grid, kThreads, smem, s>>>(ma, mb, M, N, K, y, out_mode, status);
   return cudaGetLastError();
 }
