@@ -372,18 +372,20 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
  * akv_decode_static_scratch_bytes() bytes (16 MiB) on every GPU that loads
  * the library, held until the process exits.  Nothing is allocated by the
  * call (no cudaMalloc/cudaFree, no allocating library routine).
- *  - Limit: decode_partials(B, Hq, max_kv) = B * Hq * ceil(max_kv / 2048) *
- *    66 * 4 bytes (each part rounded up to 256) must fit the array; larger
- *    requests return AKV_ERR_UNSUPPORTED with the sizes in akv_last_error(),
- *    before anything is enqueued.
+ *  - Limit: the bytes akv_decode_workspace() returns for the same shape, B
+ *    and max_kv (split-KV partials, B * Hq * ceil(max_kv / 1024) * 66 * 4
+ *    bytes, plus B * Hkv * 4 bytes of merge counters, each part rounded up
+ *    to 256) must fit the array; larger requests return
+ *    AKV_ERR_UNSUPPORTED with the sizes in akv_last_error(), before
+ *    anything is enqueued.
  *  - Set-up: the first call on a device (with that device current) looks up
  *    the array's device address with cudaGetSymbolAddress and caches it; make
  *    that first call before any stream capture.
  *  - Sharing: every call on a device uses the same array.  Calls that
  *    overlap on the GPU (other streams, other host threads) race and corrupt
  *    each other's results; serialise them.  The array keeps the last call's
- *    contents; nothing in it needs to start at zero (each call writes every
- *    partial it later reads). */
+ *    contents; the call itself clears the merge counters (a memset on
+ *    `stream`) and writes every partial it later reads. */
 akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
                                        const int32_t *q_pos, const void *k_pool,
                                        const void *v_pool, const int32_t *kv_indptr,
