@@ -664,6 +664,13 @@ akv_status plan_create_impl(const akv_shape *shape, int32_t n_req, const int32_t
     max_ver = std::max<int>(max_ver, 1 + (int)(std::unique(rb.begin(), rb.end()) - rb.begin()));
   }
   P->max_ver = max_ver;
+  // the attention kernel addresses rotated-key rows (version, KV head, slot)
+  // with one 32-bit TMA coordinate
+  if ((int64_t)max_ver * shape->Hkv * T >= (int64_t)INT32_MAX) {
+    delete P;
+    return fail(AKV_ERR_UNSUPPORTED, "key versions x KV heads x rows (%d x %d x %lld) exceed 2^31",
+                max_ver, shape->Hkv, (long long)T);
+  }
   try {
     P->tok_pos.assign(T, 0);
     P->tok_seg.assign(T, 0);

@@ -196,3 +196,16 @@ def test_shared_prefix_plan_rejects_bad_sharing(akv):
     with pytest.raises(akv.AkvError) as e:
         akv.Plan(shp, cu_for(ok), bad, share=[(-1, 0), (0, P), (0, P)])
     assert e.value.status == INVALID
+
+
+def test_plan_rejects_key_rows_beyond_32_bit_coordinates():
+    """The attention kernel addresses rotated-key rows (version, KV head,
+    slot) with one 32-bit TMA coordinate: 2 versions x 8 heads x 140M rows
+    is refused before anything is allocated."""
+    shp = akv.shape(8, 8, 64, "bf16")
+    T = 140_000_000
+    ms = np.array([0, T // 2, T], dtype=np.int32)
+    ops = [(ms, np.zeros(0, np.int32), np.zeros(0, np.int32), np.array([0], np.int32))]
+    with pytest.raises(akv.AkvError, match="UNSUPPORTED"):
+        akv.Plan(shp, [0, T], ops)
+
