@@ -198,7 +198,7 @@ def test_shared_prefix_plan_rejects_bad_sharing(akv):
     assert e.value.status == INVALID
 
 
-def test_plan_rejects_key_rows_beyond_32_bit_coordinates():
+def test_plan_rejects_key_rows_beyond_32_bit_coordinates(akv):
     """The attention kernel addresses rotated-key rows (version, KV head,
     slot) with one 32-bit TMA coordinate: 2 versions x 8 heads x 140M rows
     is refused before anything is allocated."""
