@@ -149,6 +149,17 @@ struct ParamBlob {
 static_assert(sizeof(ParamBlob) + sizeof(void *) <= 4096, "kernel parameter space");
 cudaError_t launch_param_upload(char *dst, const ParamBlob &blob, cudaStream_t s);
 
+// Larger host tables staged in mapped pinned memory, copied by a kernel that
+// reads the host block directly (the copy engine queues behind unrelated
+// copies, e.g. a caller's input transfer on another stream).
+constexpr int kUploadMaxSegs = 16;
+struct UploadSegs {
+  int32_t n;
+  ParamSeg seg[kUploadMaxSegs];
+};
+cudaError_t launch_mapped_upload(const void *src_dev, char *dst, const UploadSegs &segs,
+                                 cudaStream_t s);
+
 size_t decode_partials_bytes(int B, int Hq, int max_kv, bool rope = false);
 // partials + the per-(request, KV head) merge counters of the bf16 kernel
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv);

@@ -435,7 +435,8 @@ class PinnedPool {
     }
     Block b;
     b.bytes = align_up(std::max<size_t>(bytes, 1), size_t(1) << 20);
-    if (cudaHostAlloc((void **)&b.p, b.bytes, cudaHostAllocPortable) != cudaSuccess) {
+    if (cudaHostAlloc((void **)&b.p, b.bytes, cudaHostAllocPortable | cudaHostAllocMapped) !=
+        cudaSuccess) {
       (void)cudaGetLastError();
       return false;
     }
@@ -479,8 +480,13 @@ PinnedPool &pinned_pool() {
 // plain (blocking) copies when no pinned memory can be had.
 cudaError_t upload_async(char *dst, const HostPart *parts, int n, cudaStream_t s) {
   size_t total = 0;
-  for (int i = 0; i < n; ++i) total += align_up(parts[i].bytes, 16);
-  if (total <= (size_t)kParamBlobBytes && n <= kParamMaxSegs) {
+  bool off32 = true;  // segment offsets fit the copy kernels' 32-bit fields
+  for (int i = 0; i < n; ++i) {
+    total += align_up(parts[i].bytes, 16);
+    off32 = off32 && parts[i].dst_off + parts[i].bytes <= (size_t)UINT32_MAX;
+  }
+  off32 = off32 && total <= (size_t)UINT32_MAX;
+  if (off32 && total <= (size_t)kParamBlobBytes && n <= kParamMaxSegs) {
     ParamBlob blob;
     blob.n_seg = 0;
     size_t o = 0;
@@ -508,13 +514,31 @@ cudaError_t upload_async(char *dst, const HostPart *parts, int n, cudaStream_t s
     if (parts[i].bytes) std::memcpy(blk.p + o, parts[i].src, parts[i].bytes);
     o += align_up(parts[i].bytes, 16);
   }
-  o = 0;
+  // The block is mapped: a kernel on the stream reads it directly.  (A
+  // cudaMemcpyAsync would queue on a copy engine behind whatever the caller
+  // is transferring on other streams, e.g. the next step's inputs.)
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < n && e == cudaSuccess; ++i) {
-    if (parts[i].bytes)
-      e = cudaMemcpyAsync(dst + parts[i].dst_off, blk.p + o, parts[i].bytes,
-                          cudaMemcpyHostToDevice, s);
-    o += align_up(parts[i].bytes, 16);
+  void *dsrc = nullptr;
+  if (off32 && n <= kUploadMaxSegs && cudaHostGetDevicePointer(&dsrc, blk.p, 0) == cudaSuccess) {
+    UploadSegs segs;
+    segs.n = 0;
+    o = 0;
+    for (int i = 0; i < n; ++i) {
+      if (parts[i].bytes)
+        segs.seg[segs.n++] = ParamSeg{(uint32_t)parts[i].dst_off, (uint32_t)o,
+                                      (uint32_t)parts[i].bytes};
+      o += align_up(parts[i].bytes, 16);
+    }
+    e = launch_mapped_upload(dsrc, dst, segs, s);
+  } else {
+    (void)cudaGetLastError();
+    o = 0;
+    for (int i = 0; i < n && e == cudaSuccess; ++i) {
+      if (parts[i].bytes)
+        e = cudaMemcpyAsync(dst + parts[i].dst_off, blk.p + o, parts[i].bytes,
+                            cudaMemcpyHostToDevice, s);
+      o += align_up(parts[i].bytes, 16);
+    }
   }
   cudaEvent_t ev = nullptr;
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);

@@ -157,9 +157,42 @@ __global__ void __launch_bounds__(256) param_upload_kernel(const ParamBlob blob,
   }
 }
 
+// grid-stride copy of segments from a device-visible host block; 16 bytes
+// at a time where source, destination and length are 16-byte multiples
+__global__ void __launch_bounds__(256) mapped_upload_kernel(const uint8_t *__restrict__ src,
+                                                            char *__restrict__ dst,
+                                                            const UploadSegs segs) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int sg = 0; sg < segs.n; ++sg) {
+    const ParamSeg g = segs.seg[sg];
+    const uint8_t *s = src + g.src_off;
+    char *d = dst + g.dst_off;
+    int64_t done = 0;
+    if (((g.src_off | g.dst_off | (uintptr_t)src | (uintptr_t)dst) & 15) == 0) {
+      const int64_t n16 = g.bytes / 16;
+      for (int64_t i = tid; i < n16; i += stride)
+        reinterpret_cast<uint4 *>(d)[i] = reinterpret_cast<const uint4 *>(s)[i];
+      done = n16 * 16;
+    }
+    for (int64_t i = done + tid; i < (int64_t)g.bytes; i += stride) d[i] = (char)s[i];
+  }
+}
+
 }  // namespace
 
 int compact_blocks(int T) { return (T + kBlock - 1) / kBlock; }
+
+cudaError_t launch_mapped_upload(const void *src_dev, char *dst, const UploadSegs &segs,
+                                 cudaStream_t s) {
+  int64_t total = 0;
+  for (int i = 0; i < segs.n; ++i) total += segs.seg[i].bytes;
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total / 16 + 255) / 256;
+  const unsigned grid = (unsigned)(want < 1024 ? (want > 0 ? want : 1) : 1024);
+  mapped_upload_kernel<<<grid, 256, 0, s>>>((const uint8_t *)src_dev, dst, segs);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_param_upload(char *dst, const ParamBlob &blob, cudaStream_t s) {
   param_upload_kernel<<<1, 256, 0, s>>>(blob, dst);
