@@ -196,7 +196,10 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
     flops = float(info["visible_pairs"]) * 4 * 64 * traj.Hq
     res = dict(plan=info, plan_host_ms=plan_ms, prep_ms=prep_ms, attn_ms=attn_ms,
                device_ms_total=dev_ms, wall_s=wall, flops_per_step=flops, status=status,
-               clocks=clk.summary(), launches_per_step=4)
+               clocks=clk.summary(),
+               # per step: the plan tables' upload (a copy kernel), prep_q,
+               # prep_kv, the visibility masks, the attention kernel
+               launches_per_step=5)
     if with_e2e:
         # end to end: every step copies its inputs from pinned host memory to
         # the device, plans on the host and runs akv_segment_attention, and
