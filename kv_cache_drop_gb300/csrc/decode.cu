@@ -4,8 +4,10 @@
 //
 // Split-KV: request b's index list is cut into chunks of `chunk` keys; one CTA
 // takes (chunk, KV head g, request b) and produces a partial (row max m, row
-// sum l, unnormalised output o) for the Hq/Hkv query heads of group g; a
-// combine kernel merges the partials by their log-sum-exp.
+// sum l, unnormalised output o) for the Hq/Hkv query heads of group g; the
+// partials are merged by their log-sum-exp -- for bf16 inside the same
+// launch, by the last CTA of each (request, KV head) to finish; for fp32 by
+// a combine kernel.
 //
 // bf16: the group's query heads form the rows of an m16n8k16 tensor-core tile
 // (S = Q K^T with K rows as the B operand, then O += P V with P reused from
