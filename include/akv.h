@@ -393,6 +393,20 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
                                        akv_stream_t stream);
 size_t akv_decode_static_scratch_bytes(void);
 
+/* Debug check of decode index data.  The decode entry points trust
+ * kv_indptr / kv_indices (an out-of-range slot would be read from the pool);
+ * this call checks them on the device without reading any pool slot:
+ * kv_indptr (device int32 [B+1]) starts at 0 and every request's length is
+ * in [0, max_kv]; kv_indptr[B] <= n_indices (the entries allocated in
+ * kv_indices, device int32); every listed slot is in [0, S) (S = pool rows).
+ * Violations are OR-ed into *status (device uint32, which the caller zeroes
+ * first): bit 0 (1) the index pointer, bit 1 (2) a slot.  Asynchronous on
+ * `stream`; read *status after synchronising.  No counterpart on the pages:
+ * the check stands in for a memory checker on data the kernels trust. */
+akv_status akv_decode_check_indices(int32_t B, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                    int32_t n_indices, int32_t S, int32_t max_kv, uint32_t *status,
+                                    akv_stream_t stream);
+
 /* Append (section 3.3): for i in 0..n-1, k_pool[slot[i]] = R(pos[i]) *
  * k_new[i] and v_pool[slot[i]] = v_new[i].  k_new/v_new: device [n, Hkv, D]
  * raw; pos, slot: device int32 [n]; slots must be distinct. */

@@ -150,6 +150,8 @@ _SIGS = {
                                     [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_void_p,
                                                              ctypes.c_void_p]),
     "akv_decode_static_scratch_bytes": (ctypes.c_size_t, []),
+    "akv_decode_check_indices": (ctypes.c_int, [ctypes.c_int32] + [ctypes.c_void_p] * 2 +
+                                 [ctypes.c_int32] * 3 + [ctypes.c_void_p, ctypes.c_void_p]),
     "akv_gemm_bf16": (ctypes.c_int, [ctypes.c_int32] * 3 + [ctypes.c_void_p] * 3 +
                       [ctypes.c_int32, ctypes.c_void_p]),
     "akv_rmsnorm": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
@@ -480,6 +482,15 @@ def akv_decode_attention_static(shp: Shape, B: int, q, q_pos, k_pool, v_pool, kv
                                              _dev(k_pool), _dev(v_pool), _dev(kv_indptr),
                                              _dev(kv_indices), max_kv, _dev(out),
                                              _stream(stream)))
+
+
+def akv_decode_check_indices(B: int, kv_indptr, kv_indices, S: int, max_kv: int, status,
+                             stream=None):
+    """Device check of decode index data (see include/akv.h); ORs violation
+    bits into ``status`` (a zeroed CUDA uint32/int32 tensor of one element)."""
+    _check(lib().akv_decode_check_indices(B, _dev(kv_indptr), _dev(kv_indices),
+                                          kv_indices.numel(), S, max_kv, _dev(status),
+                                          _stream(stream)))
 
 
 def akv_decode_static_scratch_bytes() -> int:

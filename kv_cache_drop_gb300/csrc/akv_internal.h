@@ -193,6 +193,11 @@ cudaError_t launch_widen(int64_t n, const void *x, float *y, cudaStream_t s);
 
 // Decode with its split-KV partials in a static device array (no workspace).
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+// akv_decode_check_indices status bits
+constexpr uint32_t kDecodeIndptr = 1u;  // indptr[0] != 0, a negative or > max_kv length, or too many entries
+constexpr uint32_t kDecodeSlot = 2u;    // a slot outside [0, S)
+cudaError_t launch_check_indices(int B, const int32_t *indptr, const int32_t *indices, int S,
+                                 int max_kv, int64_t nnz_cap, uint32_t *status, cudaStream_t s);
 // bf16 decode: the in-kernel split merge keeps one weight per split and query
 // head of a group in shared memory (<= 1000 splits of 2048 keys)
 constexpr int kDecodeMaxKeys = 1000 * 2048;

@@ -1228,6 +1228,20 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
 
 size_t akv_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
+akv_status akv_decode_check_indices(int32_t B, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                    int32_t n_indices, int32_t S, int32_t max_kv, uint32_t *status,
+                                    akv_stream_t stream) {
+  AKV_ENTRY("akv_decode_check_indices");
+  if (B < 0 || n_indices < 0 || S < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
+  if (!kv_indptr || !status || (n_indices > 0 && !kv_indices))
+    return fail(AKV_ERR_INVALID, "NULL argument");
+  if (B == 0) return AKV_OK;
+  cudaError_t e = launch_check_indices(B, kv_indptr, kv_indices, S, max_kv, n_indices, status,
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode index check");
+  return AKV_OK;
+}
+
 // ------------------------------------------------------------------------
 // Decoder layers around the segment attention
 // ------------------------------------------------------------------------

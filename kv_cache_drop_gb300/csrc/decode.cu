@@ -817,6 +817,47 @@ cudaError_t launch_decode_rope(int dtype, int B, int Hq, int Hkv, const void *q,
 }
 
 // ---------------------------------------------------------------------------
+// Debug check of caller-provided decode index data, which the decode kernels
+// trust (an out-of-range slot would be read).  Reads only kv_indptr and
+// kv_indices; never touches a pool slot.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void check_indices_kernel(int B, const int32_t *__restrict__ indptr,
+                                     const int32_t *__restrict__ indices, int S, int max_kv,
+                                     int64_t nnz_cap, uint32_t *status) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  uint32_t bad = 0;
+  if (tid == 0 && indptr[0] != 0) bad |= kDecodeIndptr;
+  for (int64_t b = tid; b < B; b += stride) {
+    const int64_t len = (int64_t)indptr[b + 1] - indptr[b];
+    if (len < 0 || len > max_kv) bad |= kDecodeIndptr;
+  }
+  // the entries actually listed (bounded by the caller's capacity)
+  int64_t nnz = indptr[B];
+  if (nnz < 0) nnz = 0;
+  if (nnz > nnz_cap) {
+    if (tid == 0) bad |= kDecodeIndptr;
+    nnz = nnz_cap;
+  }
+  for (int64_t i = tid; i < nnz; i += stride) {
+    const int32_t slot = indices[i];
+    if (slot < 0 || slot >= S) bad |= kDecodeSlot;
+  }
+  if (bad) atomicOr(status, bad);
+}
+}  // namespace
+
+cudaError_t launch_check_indices(int B, const int32_t *indptr, const int32_t *indices, int S,
+                                 int max_kv, int64_t nnz_cap, uint32_t *status, cudaStream_t s) {
+  const int64_t work = nnz_cap > B ? nnz_cap : B;
+  const int64_t want = (work + 255) / 256;
+  const unsigned grid = (unsigned)(want < 4096 ? (want > 0 ? want : 1) : 4096);
+  check_indices_kernel<<<grid, 256, 0, s>>>(B, indptr, indices, S, max_kv, nnz_cap, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Decode without a caller workspace.  The split-KV partials go to a fixed
 // array in this module's device memory instead: every GPU that loads the
 // library keeps kStaticScratchBytes for it until the process exits.  Host

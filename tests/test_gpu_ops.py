@@ -280,6 +280,38 @@ def test_decode_many_splits():
     assert_close(res[0], _decode_oracle(dw, 0, oracle.widen(dw.q[0], "bf16")), "bf16")
 
 
+def test_decode_index_check():
+    """The debug check of decode index data (reads only the index arrays):
+    clean on a real workload; flags a slot outside the pool, a negative slot,
+    a non-monotone index pointer, a request longer than max_kv, and an index
+    pointer running past the entries given."""
+    torch = _torch()
+    dw = workloads.decode_workload(seed=16, B=3, active=(100, 2000), steps=1, Hq=8, Hkv=2)
+    indptr, idx = dw.indices_at(0)
+    S = int(dw.k_pool.shape[0])
+    max_kv = int(np.max(np.diff(indptr)))
+
+    def check(ip, ix, s_rows, mk):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        akv.akv_decode_check_indices(len(ip) - 1, akv.i32_device(ip), akv.i32_device(ix), s_rows,
+                                     mk, st)
+        torch.cuda.synchronize()
+        return int(st.item())
+
+    assert check(indptr, idx, S, max_kv) == 0
+    bad = np.array(idx, copy=True)
+    bad[len(bad) // 2] = S  # one past the pool
+    assert check(indptr, bad, S, max_kv) == 2
+    bad = np.array(idx, copy=True)
+    bad[0] = -1
+    assert check(indptr, bad, S, max_kv) == 2
+    ip = np.array(indptr, copy=True)
+    ip[1], ip[2] = ip[2], ip[1]  # request 0 longer, request 1 negative
+    assert check(ip, idx, S, max_kv) & 1
+    assert check(indptr, idx, S, max_kv - 1) == 1  # a request longer than max_kv
+    assert check(indptr, np.array(idx[:-5]), S, max_kv) == 1  # indptr[B] past the entries
+
+
 def test_decode_full_size_steps():
     """14 requests, 20k-90k active keys each, 256 decode steps with appends;
     steps 0, 1 and 255 checked in full."""
