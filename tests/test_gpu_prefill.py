@@ -86,6 +86,20 @@ def test_prefill_rolling_drop_full_size():
     assert np.isfinite(got).all()
 
 
+def test_prefill_rolling_drop_48k_truncation():
+    """The same trajectory cut at the first message boundary at or after
+    49,152 tokens (the "~48k" reading of the workload), sampled rows, with a
+    peaky query variant on the same rows."""
+    r = workloads.rolling_drop_config(truncate_at_boundary=49152)
+    assert 49152 <= r.T < 49152 + 3000
+    got, _, _ = run_prefill([r])
+    rows = sample_rows(r, 12, seed=3)
+    assert_close(got[rows], oracle_rows(r, rows), "bf16")
+    rp = workloads.rolling_drop_config(truncate_at_boundary=49152, q_scale=8.0)
+    got_p, _, _ = run_prefill([rp])
+    assert_close(got_p[rows], oracle_rows(rp, rows), "bf16", max_abs=BF16_PEAKY_MAX_ABS)
+
+
 def test_prefill_repos_full_size():
     """128k tokens with a repos at 96k: both key versions, sampled rows."""
     r = workloads.repos_config()
