@@ -131,6 +131,11 @@ struct CompactDev {
 cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *active_pos,
                            cudaStream_t s);
 int compact_blocks(int T);
+// the same from the kept runs (host tables, nk <= repos_inline_runs(), n >= 1
+// compacted entries), one launch with the tables in its parameters
+cudaError_t launch_compact_runs(int n, int nk, const int32_t *kstart, const int32_t *kprefix,
+                                const int32_t *kpos, int32_t *active_idx, int32_t *active_pos,
+                                cudaStream_t s);
 
 // Small host tables delivered as the parameters of a copy kernel on the
 // stream: a launch costs far less latency than starting the copy engine for

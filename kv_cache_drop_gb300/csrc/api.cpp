@@ -933,49 +933,6 @@ size_t compact_ws_bytes(int n_msgs, int T) {
 }
 }  // namespace
 
-size_t akv_compact_workspace(const akv_oplog *ops, int32_t T) {
-  if (!ops || ops->n_msgs < 0) return 0;
-  return compact_ws_bytes(ops->n_msgs, T);
-}
-
-akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *active_idx,
-                       int32_t *active_pos, int32_t *n_active, void *workspace,
-                       size_t workspace_bytes, akv_stream_t stream) {
-  AKV_ENTRY("akv_compact");
-  if (akv_status st = check_oplog(ops, T, 0)) return st;
-  if (!n_active || !active_idx || !active_pos) return fail(AKV_ERR_INVALID, "NULL output");
-  CompactHost c;
-  if (akv_status st = compact_host(ops, upto, &c)) return st;
-  *n_active = (int32_t)c.n_active;
-  if (c.T_upto == 0) return AKV_OK;
-  const size_t need = compact_ws_bytes(ops->n_msgs, T);
-  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
-    return fail(AKV_ERR_WORKSPACE, "compact workspace: need %zu aligned bytes", need);
-  cudaStream_t s = (cudaStream_t)stream;
-  char *b = (char *)workspace;
-  size_t o0 = 0, o1 = align_up(4 * (size_t)(ops->n_msgs + 1), 256);
-  size_t o2 = o1 + align_up((size_t)ops->n_msgs + 1, 256);
-  size_t o3 = o2 + align_up((size_t)ops->n_msgs + 1, 256);
-  const HostPart parts[] = {{o0, ops->msg_start, 4 * (size_t)(c.n_msgs + 1)},
-                            {o1, c.keep.data(), (size_t)c.n_msgs},
-                            {o2, c.alive_br.data(), (size_t)c.n_msgs}};
-  cudaError_t e = upload_async(b, parts, 3, s);
-  if (e != cudaSuccess) return cuda_fail(e, "compact upload");
-  CompactDev d{};
-  d.msg_start = (const int32_t *)(b + o0);
-  d.keep = (const uint8_t *)(b + o1);
-  d.alive_br = (const uint8_t *)(b + o2);
-  d.block_cnt = (int32_t *)(b + o3);
-  d.n_msgs = c.n_msgs;
-  d.T = c.T_upto;
-  d.br_end = c.br_end;
-  d.r = c.r;
-  d.has_br = c.has_br;
-  e = launch_compact(d, active_idx, active_pos, s);
-  if (e != cudaSuccess) return cuda_fail(e, "compact");
-  return AKV_OK;
-}
-
 namespace {
 // Survivors after the drops of boundary `upto`, as runs of kept messages:
 // first row, first compacted index (exclusive prefix of kept lengths, with
@@ -1000,6 +957,62 @@ void kept_runs(const akv_oplog *o, const CompactHost &c, std::vector<int32_t> *k
   kprefix->push_back(j);
 }
 }  // namespace
+
+size_t akv_compact_workspace(const akv_oplog *ops, int32_t T) {
+  if (!ops || ops->n_msgs < 0) return 0;
+  return compact_ws_bytes(ops->n_msgs, T);
+}
+
+akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *active_idx,
+                       int32_t *active_pos, int32_t *n_active, void *workspace,
+                       size_t workspace_bytes, akv_stream_t stream) {
+  AKV_ENTRY("akv_compact");
+  if (akv_status st = check_oplog(ops, T, 0)) return st;
+  if (!n_active || !active_idx || !active_pos) return fail(AKV_ERR_INVALID, "NULL output");
+  CompactHost c;
+  if (akv_status st = compact_host(ops, upto, &c)) return st;
+  *n_active = (int32_t)c.n_active;
+  if (c.T_upto == 0) return AKV_OK;
+  const size_t need = compact_ws_bytes(ops->n_msgs, T);
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < need)
+    return fail(AKV_ERR_WORKSPACE, "compact workspace: need %zu aligned bytes", need);
+  if (c.n_active == 0) return AKV_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  {
+    std::vector<int32_t> kstart, kprefix, kpos;
+    kept_runs(ops, c, &kstart, &kprefix, &kpos);
+    const int nk = (int)kstart.size();
+    if (nk <= repos_inline_runs()) {  // one launch, the run tables in its parameters
+      cudaError_t e = launch_compact_runs((int)c.n_active, nk, kstart.data(), kprefix.data(),
+                                          kpos.data(), active_idx, active_pos, s);
+      if (e != cudaSuccess) return cuda_fail(e, "compact");
+      return AKV_OK;
+    }
+  }
+  char *b = (char *)workspace;
+  size_t o0 = 0, o1 = align_up(4 * (size_t)(ops->n_msgs + 1), 256);
+  size_t o2 = o1 + align_up((size_t)ops->n_msgs + 1, 256);
+  size_t o3 = o2 + align_up((size_t)ops->n_msgs + 1, 256);
+  const HostPart parts[] = {{o0, ops->msg_start, 4 * (size_t)(c.n_msgs + 1)},
+                            {o1, c.keep.data(), (size_t)c.n_msgs},
+                            {o2, c.alive_br.data(), (size_t)c.n_msgs}};
+  cudaError_t e = upload_async(b, parts, 3, s);
+  if (e != cudaSuccess) return cuda_fail(e, "compact upload");
+  CompactDev d{};
+  d.msg_start = (const int32_t *)(b + o0);
+  d.keep = (const uint8_t *)(b + o1);
+  d.alive_br = (const uint8_t *)(b + o2);
+  d.block_cnt = (int32_t *)(b + o3);
+  d.n_msgs = c.n_msgs;
+  d.T = c.T_upto;
+  d.br_end = c.br_end;
+  d.r = c.r;
+  d.has_br = c.has_br;
+  e = launch_compact(d, active_idx, active_pos, s);
+  if (e != cudaSuccess) return cuda_fail(e, "compact");
+  return AKV_OK;
+}
+
 
 size_t akv_repos_boundary_workspace(const akv_oplog *ops, int32_t T) {
   if (!ops || ops->n_msgs < 0) return 0;

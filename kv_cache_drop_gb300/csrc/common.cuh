@@ -185,4 +185,31 @@ __device__ __forceinline__ bool rotate_pair(const Tin *src, Tout *dst, int c, co
   return !(big <= 65504.f);
 }
 
+// Survivors of a boundary as runs of kept messages, small enough to travel
+// in a kernel's parameters (__grid_constant__): t = kstart[nk] |
+// kprefix[nk + 1] | kpos[nk] -- first row of each run, its first compacted
+// index (exclusive prefix of run lengths, total appended), position of its
+// first row before the boundary's repos.
+constexpr int kInlineRuns = 256;
+struct KeptRunTable {
+  int nk;
+  int32_t t[3 * kInlineRuns + 1];
+  __device__ __forceinline__ int32_t kstart(int run) const { return t[run]; }
+  __device__ __forceinline__ int32_t kpos(int run) const { return t[2 * nk + 1 + run]; }
+  // run holding compacted index j (0 <= j < total) and j's offset in it
+  __device__ __forceinline__ void find(int j, int *run, int *off) const {
+    const int32_t *kprefix = t + nk;
+    int lo = 0, hi = nk;  // kprefix[lo] <= j < kprefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (kprefix[mid] <= j) lo = mid; else hi = mid;
+    }
+    *run = lo;
+    *off = j - kprefix[lo];
+  }
+};
+// fills rt from the host run tables; false unless 1 <= nk <= kInlineRuns
+bool fill_run_table(KeptRunTable *rt, int nk, const int32_t *kstart, const int32_t *kprefix,
+                    const int32_t *kpos);
+
 }  // namespace akv

@@ -8,6 +8,11 @@
 // the survivors of the last repos, or r + offset for later appends).  Two
 // launches: per-block counts, then per-block prefix (over the few preceding
 // block counts) + block scan + scatter.  Bit-exact integer work.
+//
+// Since both flags are per message, the survivors are runs of whole kept
+// messages whose positions are consecutive within a run; when there are few
+// runs the host passes them in the kernel's parameters and one launch
+// expands them, one thread per compacted index (compact_runs_kernel).
 #include "common.cuh"
 
 namespace akv {
@@ -149,6 +154,19 @@ __global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev cg, 
   }
 }
 
+// thread = compacted index j: its run by binary search over the run table
+// (lanes of a warp mostly share a run, so the parameter reads broadcast)
+__global__ void __launch_bounds__(kThreads)
+    compact_runs_kernel(int n, const __grid_constant__ KeptRunTable rt, int32_t *__restrict__ active_idx,
+                        int32_t *__restrict__ active_pos) {
+  const int j = blockIdx.x * kThreads + threadIdx.x;
+  if (j >= n) return;
+  int run, off;
+  rt.find(j, &run, &off);
+  active_idx[j] = rt.kstart(run) + off;
+  active_pos[j] = rt.kpos(run) + off;
+}
+
 __global__ void __launch_bounds__(256) param_upload_kernel(const ParamBlob blob, char *dst) {
   for (int sg = 0; sg < blob.n_seg; ++sg) {
     const ParamSeg g = blob.seg[sg];
@@ -204,6 +222,16 @@ cudaError_t launch_compact(const CompactDev &c, int32_t *active_idx, int32_t *ac
   const int nb = compact_blocks(c.T);
   compact_count_kernel<<<nb, kThreads, 0, s>>>(c);
   compact_write_kernel<<<nb, kThreads, 0, s>>>(c, active_idx, active_pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_runs(int n, int nk, const int32_t *kstart, const int32_t *kprefix,
+                                const int32_t *kpos, int32_t *active_idx, int32_t *active_pos,
+                                cudaStream_t s) {
+  KeptRunTable rt;
+  if (n < 1 || !fill_run_table(&rt, nk, kstart, kprefix, kpos)) return cudaErrorInvalidValue;
+  compact_runs_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(n, rt, active_idx,
+                                                                                     active_pos);
   return cudaGetLastError();
 }
 

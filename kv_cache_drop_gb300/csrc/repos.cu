@@ -108,22 +108,14 @@ struct KeptRuns {
 };
 
 // rows of akv_repos_boundary with the run tables carried in the kernel's
-// parameters (no upload), for up to kInlineRuns runs: kstart[nk] |
-// kprefix[nk + 1] | kpos[nk]
-constexpr int kInlineRuns = 256;
+// parameters (no upload)
 struct KeptRunsInline {
-  int nk;
-  int32_t t[3 * kInlineRuns + 1];
+  KeptRunTable tab;
   __device__ __forceinline__ void get(int j, int64_t *in, int32_t *delta) const {
-    const int32_t *kstart = t, *kprefix = t + nk, *kpos = t + 2 * nk + 1;
-    int lo = 0, hi = nk;  // kprefix[lo] <= j < kprefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (kprefix[mid] <= j) lo = mid; else hi = mid;
-    }
-    const int off = j - kprefix[lo];
-    *in = kstart[lo] + off;
-    *delta = j - (kpos[lo] + off);
+    int run, off;
+    tab.find(j, &run, &off);
+    *in = tab.kstart(run) + off;
+    *delta = j - (tab.kpos(run) + off);
   }
 };
 
@@ -238,19 +230,24 @@ cudaError_t launch_repos_boundary(int dtype, int Hkv, int r, int nk, const int32
 }
 
 int repos_inline_runs() { return kInlineRuns; }
+bool fill_run_table(KeptRunTable *rt, int nk, const int32_t *kstart, const int32_t *kprefix,
+                    const int32_t *kpos) {
+  if (nk < 1 || nk > kInlineRuns) return false;
+  rt->nk = nk;
+  for (int i = 0; i < nk; ++i) {
+    rt->t[i] = kstart[i];
+    rt->t[2 * nk + 1 + i] = kpos[i];
+  }
+  for (int i = 0; i <= nk; ++i) rt->t[nk + i] = kprefix[i];
+  return true;
+}
 
 cudaError_t launch_repos_boundary_inline(int dtype, int Hkv, int r, int nk, const int32_t *kstart,
                                          const int32_t *kprefix, const int32_t *kpos,
                                          const void *kin, const void *vin, void *kout, void *vout,
                                          const RopeTheta &th, cudaStream_t s) {
-  if (nk < 1 || nk > kInlineRuns) return cudaErrorInvalidValue;
   KeptRunsInline rs;
-  rs.nk = nk;
-  for (int i = 0; i < nk; ++i) {
-    rs.t[i] = kstart[i];
-    rs.t[2 * nk + 1 + i] = kpos[i];
-  }
-  for (int i = 0; i <= nk; ++i) rs.t[nk + i] = kprefix[i];
+  if (!fill_run_table(&rs.tab, nk, kstart, kprefix, kpos)) return cudaErrorInvalidValue;
   if (dtype == AKV_F32) return repos_stream<float>(Hkv, r, rs, kin, vin, kout, vout, th, s);
   return repos_stream<__nv_bfloat16>(Hkv, r, rs, kin, vin, kout, vout, th, s);
 }
