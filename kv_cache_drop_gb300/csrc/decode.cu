@@ -121,7 +121,17 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // and S = qhi k + qlo k in fp16 MMAs.  Rotated keys must lie within the fp16
 // range (|k| < 65504; a larger one gives inf).  The append is then a plain
 // copy.
+// The angles: a request's entries are in position order and mostly close
+// together, so per tile lane f forms cos/sin(p0 theta_f) once for the tile's
+// first position p0, and a key at p = p0 + delta, 0 <= delta < kDeltas,
+// takes it rotated by delta theta_f (angle addition) from a per-CTA table
+// of cos/sin(delta theta_f); other keys compute their angles directly.
 constexpr int kStageBytes(bool rope) { return rope ? 4096 + 64 : 4096; }
+constexpr int kDeltas = 64;
+// table row: for frequency pair j = f / 2, float4 (cos f, sin f, cos f+1,
+// sin f+1); rows padded to 20 float4 so that the two rows read by one
+// 8-lane phase of a 16-byte load fall in different banks
+constexpr int kDeltaRow = kD / 4 + 4;
 
 // cos/sin of pos * theta by the fast sin/cos instructions (absolute error
 // about 4e-7 on the reduced angle, |r| <= pi)
@@ -143,6 +153,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float cs[kD / 2], sn[kD / 2];
   __shared__ ThetaSmem ts;
+  __shared__ float4 dtab[kRope ? kDeltas * kDeltaRow : 1];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int ns = gridDim.x;
   const int grp = Hq / Hkv;
@@ -158,7 +169,25 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   }
 
   if (threadIdx.x < kD / 2) rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
-  if (kRope) stage_theta(th, ts);
+  if (kRope) {
+    stage_theta(th, ts);
+    // delta table: thread = (frequency f, block of 16 deltas); the block's
+    // first entry directly, then 15 steps of the delta = 1 rotation
+    for (int u = threadIdx.x; u < (kD / 2) * (kDeltas / 16); u += blockDim.x) {
+      const int f = u % (kD / 2), d0 = 16 * (u / (kD / 2));
+      float c, sv, c1, s1;
+      rope_cs_pair(th.hi[f], th.lo[f], d0, &c, &sv);
+      rope_cs_pair(th.hi[f], th.lo[f], 1, &c1, &s1);
+      float *row = reinterpret_cast<float *>(dtab) + 4 * (f >> 1) + 2 * (f & 1);
+      for (int i = 0; i < 16; ++i) {
+        row[(d0 + i) * 4 * kDeltaRow] = c;
+        row[(d0 + i) * 4 * kDeltaRow + 1] = sv;
+        const float cn = c * c1 - sv * s1;
+        sv = sv * c1 + c * s1;
+        c = cn;
+      }
+    }
+  }
   __syncthreads();
   if (new_slot && c1 == n) {  // fused append of the step's token (head g)
     const int64_t src = ((int64_t)b * Hkv + g) * kD, dst = ((int64_t)new_slot[b] * Hkv + g) * kD;
@@ -297,6 +326,23 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     if (kRope) {
       const int32_t *tpos = reinterpret_cast<const int32_t *>(wsm + (it % kStages) * kSB + 4096);
       const int pa = tpos[gid], pb = tpos[gid + 8];
+      // cos/sin(p0 theta_lane) at the tile's first position
+      const int p0 = tpos[0];
+      float cb, sb;
+      if (p0 < -262144 || p0 > 262144) rope_cs(th.th[lane], (double)p0, &cb, &sb);
+      else rope_cs_fast(ts.hi[lane], ts.lo[lane], p0, &cb, &sb);
+      // the base angles of this lane's frequencies f = 16ks + 8h + 2tig and f + 1
+      float bc[2][2][2], bs[2][2][2];  // [ks][h][f or f + 1]
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int f = ks * 16 + 8 * h + 2 * tig + e;
+            bc[ks][h][e] = __shfl_sync(0xffffffffu, cb, f);
+            bs[ks][h][e] = __shfl_sync(0xffffffffu, sb, f);
+          }
       uint32_t kb[4][4];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
@@ -311,8 +357,17 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
           const int pos = (r >> 1) ? pb : pa;
           const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
+          const float cb0 = bc[ks][r & 1][0], sb0 = bs[ks][r & 1][0];
+          const float cb1 = bc[ks][r & 1][1], sb1 = bs[ks][r & 1][1];
           float c0f, s0f, c1f, s1f;
-          if (pos < -262144 || pos > 262144) {
+          const unsigned delta = (unsigned)pos - (unsigned)p0;  // wraps when pos < p0
+          if (delta < (unsigned)kDeltas) {
+            const float4 t = dtab[delta * kDeltaRow + (f >> 1)];
+            c0f = cb0 * t.x - sb0 * t.y;
+            s0f = sb0 * t.x + cb0 * t.y;
+            c1f = cb1 * t.z - sb1 * t.w;
+            s1f = sb1 * t.z + cb1 * t.w;
+          } else if (pos < -262144 || pos > 262144) {
             rope_cs(th.th[f], (double)pos, &c0f, &s0f);
             rope_cs(th.th[f + 1], (double)pos, &c1f, &s1f);
           } else {

@@ -407,6 +407,25 @@ def test_decode_rope_small(dtype):
         assert np.array_equal(got, new.reshape(-1, dw.Hkv, 64))  # raw rows, bit for bit
 
 
+def test_decode_rope_sparse_and_large_positions():
+    """Keys whose angles the kernel cannot take from its tile's first
+    position (gaps of 64 positions or more within a 16-key tile), and
+    positions past 2^18 (the double-precision angle path): request 0 at a
+    sparse random subset of 0..2e6, request 1 in runs of 10 positions 100
+    apart, request 2 dense, starting at 300,000."""
+    dw = workloads.decode_workload(seed=21, B=3, active=(300, 3000), steps=2, Hq=8, Hkv=2)
+    rng = np.random.default_rng(22)
+    n = [len(a) for a in dw.active_slots]
+    runs = (100 * np.arange((n[1] + 9) // 10)[:, None] + np.arange(10)[None, :]).reshape(-1)
+    pos = [np.sort(rng.choice(2_000_000, size=n[0], replace=False)).astype(np.int32),
+           runs[:n[1]].astype(np.int32),
+           (300_000 + np.arange(n[2])).astype(np.int32)]
+    res, _, _ = _run_decode_rope(dw, {0, 1}, pos)
+    for step, got in res.items():
+        assert_close(got, _decode_rope_oracle(dw, step, pos, oracle.widen(dw.q[step], "bf16")),
+                     "bf16")
+
+
 def test_decode_rope_repos_by_positions():
     """A repos mid-decode done by rewriting positions only (entries renumbered
     0..n-1, keys untouched): matches fp64 with the keys rotated at the new
