@@ -37,6 +37,37 @@ def test_compact_every_boundary_bit_exact(seed):
         np.testing.assert_array_equal(gp, op)
 
 
+@pytest.mark.parametrize("runs", [255, 256, 257])
+def test_compact_run_table_limit(runs):
+    """Kept runs at the limit of what the compaction kernel's parameters
+    carry (256) and one past it (the uploaded-table path): every other one
+    of 2 * runs messages dropped, so each survivor run is one message."""
+    n = 2 * runs
+    lens = np.random.default_rng(runs).integers(1, 7, size=n)
+    ms = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    drops = [(n - 1, j) for j in range(1, n, 2)]
+    r = workloads.gen._trajectory("runs", 3, ms, ["m"] * n, drops, [], 4, 2, 64, "bf16")
+    gi, gp = _compact(r.ops(), r.T, n - 1)
+    ou, op = oracle.compact(*r.ops(), upto=n - 1)
+    assert len(ou) == int(lens[0::2].sum())
+    np.testing.assert_array_equal(gi, ou)
+    np.testing.assert_array_equal(gp, op)
+
+
+def test_compact_everything_dropped():
+    """A boundary after which no token survives: zero entries, nothing
+    written; the boundary before it still compacts."""
+    ms = np.array([0, 5, 9, 16], dtype=np.int32)
+    drops = [(2, 0), (2, 1), (2, 2)]
+    r = workloads.gen._trajectory("gone", 4, ms, ["m"] * 3, drops, [], 4, 2, 64, "bf16")
+    gi, gp = _compact(r.ops(), r.T, 2)
+    assert len(gi) == 0 and len(gp) == 0
+    gi, gp = _compact(r.ops(), r.T, 1)
+    ou, op = oracle.compact(*r.ops(), upto=1)
+    np.testing.assert_array_equal(gi, ou)
+    np.testing.assert_array_equal(gp, op)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_repos_rotate(dtype):
     torch = _torch()
