@@ -70,8 +70,8 @@ struct __align__(1024) Smem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint8_t ones[kTileBytes];     // fp16 1.0, right after v: second MN atom of the PV B operand
-  uint64_t bar_kv[kStages], bar_empty[kStages];
-  uint64_t bar_s[2], bar_o[2], bar_done;
+  uint64_t bar_kv[kStages];
+  uint64_t bar_s[2], bar_done;
   uint32_t tmem_base;
 };
 
@@ -105,14 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (int)p.T;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&sm.bar_kv[s], 1);
-      ptx::mbar_init(&sm.bar_empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&sm.bar_s[i], 1);
-      ptx::mbar_init(&sm.bar_o[i], 1);
-    }
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(&sm.bar_kv[s], 1);
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(&sm.bar_s[i], 1);
     ptx::mbar_init(&sm.bar_done, 1);
     ptx::fence_barrier_init();
   }
@@ -136,7 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop (named barriers count all 32 lanes);
     // lane 0 issues the copies.  The producer takes part in every
     // generation of both P barriers, so it cannot run ahead of them; it
-    // refills the stage of window n-1 while window n is in flight.
+    // refills the stage of window n-1 while window n is in flight.  That
+    // stage is free without a wait: generation n+1 of P_1 completes only
+    // after softmax group 1 has seen S_1(n) complete, and the commit that
+    // signalled S_1(n) tracks every MMA issued before it, P_1.V(n-1) -- the
+    // last reader of the stage -- included.
     const int krow = (qt.ver * p.Hkv + g) * T, vrow = g * T;
     auto load = [&](int n) {
       if (lane == 0) {
@@ -157,10 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::named_bar_sync(kBarP + 0, kBarPCount);
       ptx::named_bar_sync(kBarP + 1, kBarPCount);
       const int m = n - 1 + kStages;  // refill the stage of window n-1
-      if (n >= 1 && m < n_win) {
-        wait_bar(&sm.bar_empty[(n - 1) % kStages], ((n - 1) / kStages) & 1, p.status);
-        load(m);
-      }
+      if (n >= 1 && m < n_win) load(m);
     }
     // every copy was waited for above: none is in flight when the CTA exits
   } else if (warp == kMmaWarp) {
@@ -197,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < 8; ++kk)
         ptx::mma_f16_ts(tmem + 256 + 80 * i, tmem + 128 * i + 8 * kk, vd + 128 * kk, idO,
                         (acc || kk > 0) ? 1u : 0u);
-      ptx::mma_commit(&sm.bar_o[i]);
     };
     ptx::named_bar_sync(kBarP + 0, kBarPCount);  // Q_0 in TMEM, window 0 landed
     ptx::named_bar_sync(kBarP + 1, kBarPCount);  // Q_1 in TMEM
@@ -215,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       issue_o(1, st, n > 0);
       if (n + 1 < n_win) issue_s(1, st1);
-      if (leader) ptx::mma_commit(&sm.bar_empty[st]);
     }
     if (leader) ptx::mma_commit(&sm.bar_done);
     wait_bar(&sm.bar_done, 0, p.status);
@@ -344,10 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st16(tS + 16 * qtr, pw);
       }
       if (n > 0 && any) {  // rare: the running max grew by more than 2^8
-        // O may be rescaled only once PV(n-1) has completed; PV(n-1) was
-        // issued before S(n), so this wait returns at once
-        wait_bar(&sm.bar_o[i], (n - 1) & 1, p.status);
-        ptx::tc_fence_after();
+        // O may be rescaled only once PV(n-1) has completed: it has, since
+        // the commit that signalled S(n) tracks every MMA issued before it
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
           uint32_t o[32];
@@ -374,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // current one has all its arrivals, even after a timed-out wait
       ptx::named_bar_sync(kBarP + i, kBarPCount);
     }
-    wait_bar(&sm.bar_o[i], (n_win - 1) & 1, p.status);
+    wait_bar(&sm.bar_done, 0, p.status);  // the last PV
     ptx::tc_fence_after();
     uint32_t o[64], lsum[16];
     ptx::tmem_ld32(tO, o);
