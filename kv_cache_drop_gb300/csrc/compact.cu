@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(kThreads) compact_write_kernel(CompactDev cg, 
 __global__ void __launch_bounds__(kThreads)
     compact_runs_kernel(int n, const __grid_constant__ KeptRunTable rt, int32_t *__restrict__ active_idx,
                         int32_t *__restrict__ active_pos) {
-  const int j = blockIdx.x * kThreads + threadIdx.x;
-  if (j >= n) return;
+  const int64_t jj = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (jj >= n) return;
+  const int j = (int)jj;
   int run, off;
   rt.find(j, &run, &off);
   active_idx[j] = rt.kstart(run) + off;
@@ -230,8 +231,8 @@ cudaError_t launch_compact_runs(int n, int nk, const int32_t *kstart, const int3
                                 cudaStream_t s) {
   KeptRunTable rt;
   if (n < 1 || !fill_run_table(&rt, nk, kstart, kprefix, kpos)) return cudaErrorInvalidValue;
-  compact_runs_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(n, rt, active_idx,
-                                                                                     active_pos);
+  const unsigned grid = (unsigned)(((int64_t)n + kThreads - 1) / kThreads);
+  compact_runs_kernel<<<grid, kThreads, 0, s>>>(n, rt, active_idx, active_pos);
   return cudaGetLastError();
 }
 
