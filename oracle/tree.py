@@ -16,6 +16,13 @@ and every question is answered by looking such names up in flat
 dictionaries.  The readings it shares with the library (which copy counts as
 "at the right positions", eviction order) are the ones written in the
 header comment of the library's tree API.
+
+Pins: hand-worked cases from the page's rules, independent of both this
+model and the library -- Figure 5's three histories, rotate / reuse / restore
+after a repos, and the four eviction rules (dropped before finished, nothing
+a running request or restore reads is freed, placeholders keep the path,
+position versions evicted separately) -- run against this model as well as
+against the library.
 """
 from __future__ import annotations
 

@@ -32,14 +32,21 @@ def _hist(msgs, drops=(), repos=()):
 A, B, C = [1, 2, 3], [4, 5], [6, 7, 8, 9]
 
 
-def test_figure5_histories_branch(akv):
+@pytest.fixture(params=["library", "model"])
+def tree(request, akv):
+    """The library's tree, or the model in oracle/tree.py: the hand-derived
+    cases below hold for both."""
+    return akv.Tree() if request.param == "library" else TreeModel()
+
+
+def test_figure5_histories_branch(tree):
     """Figure 5: (1) A, B, C then drop A; (2) A, B, drop A, then C; (3) B, C.
     (1) and (2) share A and B; C differs in all three; B of (3) is a
     separate branch."""
     h1 = _hist([A, B, C], drops=[(2, 0)])
     h2 = _hist([A, B, C], drops=[(1, 0)])
     h3 = _hist([B, C])
-    t = akv.Tree()
+    t = tree
     t.insert(*h1, 1)
     # (2) after (1): A and B are there, the drop of A after B is not
     m = t.match(*h2)
@@ -56,14 +63,14 @@ def test_figure5_histories_branch(akv):
         assert r["kind"] == "reuse" and r["prefill_tokens"] == 0
 
 
-def test_repos_copies_and_rotation(akv):
+def test_repos_copies_and_rotation(tree):
     """A repos opens a new position version.  A cached history that now
     ends with a repos needs its survivors at new positions: converted by
     rotation.  Once that history ran, the re-rotated copies exist and are
     reused as is; evicted, the state must be restored.  A message whose
     positions a repos does not change is reused as is."""
     X, Y, Z = [1] * 5, [2] * 7, [3] * 4
-    t = akv.Tree()
+    t = tree
     t.insert(*_hist([X, Y], drops=[(1, 0)]), 1)              # X dropped after Y, no repos
     with_repos = _hist([X, Y], drops=[(1, 0)], repos=[1])    # same, then a repos: Y -> 0..6
     m = t.match(*with_repos)
@@ -150,3 +157,108 @@ def test_random_operations_match_reference(akv, seed):
             want = int(rng.integers(1, 20))
             assert t.evict(want) == ref.evict(want), step
         assert t.stats() == ref.stats(), step
+
+
+# --- drop-aware eviction, pinned to the rules of the paper review page,
+# section 4.2 ("drop-aware eviction") and Appendix A.1.2:
+#   (1) physical KV is freed only when no running computation or restore
+#       still uses it -- and KV a running request no longer uses (it dropped
+#       it) is reclaimable before that request ends;
+#   (2) dropped KV is evicted before the KV of finished requests (the latter
+#       is likely to be reused by the next round);
+#   (3) tree nodes stay as empty placeholders, so what lies below them stays
+#       reachable;
+#   (4) each position version is evicted on its own.
+# The expected values below are worked out by hand from these rules; each
+# case runs against the library's tree and against the model in
+# oracle/tree.py.
+
+P_, Q_, R_, S_ = [11] * 6, [12] * 5, [13] * 4, [14] * 3
+
+
+def test_evict_dropped_before_finished(tree):
+    """A finished request's KV was used longer ago than a dropped message, so
+    an order by age alone would take it first; rule (2) takes the dropped
+    message first."""
+    done = _hist([R_, S_])                        # request 1: nothing dropped
+    tree.insert(*done, 1)
+    tree.finish(1)
+    dropped = _hist([P_, Q_], drops=[(1, 0)])     # request 2: P dropped after Q
+    tree.insert(*dropped, 2)
+    tree.finish(2)
+    assert tree.evict(len(P_)) == len(P_)
+    # P is gone (a history that needs it must restore); R, S and Q are kept
+    assert tree.match(*_hist([P_]))["kind"] == "restore"
+    assert tree.match(*done)["kind"] == "reuse"
+    assert tree.match(*dropped)["kind"] == "reuse"
+    # next: the finished request's units, oldest insert first (R, S), then Q
+    assert tree.evict(len(R_)) == len(R_)
+    assert tree.match(*done)["kind"] == "restore"
+    assert tree.match(*dropped)["kind"] == "reuse"
+
+
+def test_evict_never_frees_what_a_running_request_uses(tree):
+    """Rule (1): everything a running request reads at the end of its
+    history stays resident, however much is asked for; what it dropped is
+    freed while it still runs."""
+    h = _hist([P_, Q_, R_], drops=[(1, 0)])       # P dropped after Q; Q, R active
+    tree.insert(*h, 7)
+    assert tree.evict(10 ** 9) == len(P_)         # only the dropped P
+    st = tree.stats()
+    assert st["resident_tokens"] == len(Q_) + len(R_) == st["pinned_tokens"]
+    assert tree.match(*h)["kind"] == "reuse"
+    assert tree.evict(10 ** 9) == 0
+    tree.finish(7)                                # no longer in use: all of it goes
+    assert tree.evict(10 ** 9) == len(Q_) + len(R_)
+    assert tree.stats()["resident_tokens"] == 0
+
+
+def test_restore_in_progress_holds_its_kv(tree):
+    """A request restoring an evicted state holds it while the restore runs
+    (it is inserted, so it pins what it reads): eviction during the restore
+    frees none of it."""
+    h = _hist([P_, Q_])
+    tree.insert(*h, 1)
+    tree.finish(1)
+    assert tree.evict(10 ** 9) == len(P_) + len(Q_)
+    assert tree.match(*h)["kind"] == "restore"
+    tree.insert(*h, 2)                            # the restore runs
+    assert tree.evict(10 ** 9) == 0
+    assert tree.match(*h)["kind"] == "reuse"
+
+
+def test_evicted_nodes_stay_as_placeholders(tree):
+    """Rule (3): with the KV of the first messages evicted, their nodes still
+    lead to the later messages: a longer history still matches all of its
+    messages and needs only the evicted part restored."""
+    h = _hist([P_, Q_, R_])
+    tree.insert(*_hist([P_]), 1)
+    tree.finish(1)
+    tree.insert(*h, 2)                            # P held again, then Q, R
+    tree.finish(2)
+    nodes = tree.stats()["nodes"]
+    assert tree.evict(len(P_)) == len(P_)         # same insert: P is the oldest
+    assert tree.stats()["nodes"] == nodes
+    m = tree.match(*h)
+    assert m["matched_msgs"] == 3 and m["kind"] == "restore"
+    assert m["restore_tokens"] == len(P_) and m["reuse_tokens"] == len(Q_) + len(R_)
+
+
+def test_position_versions_evicted_separately(tree):
+    """Rule (4): Q at its first positions and Q re-numbered by a repos are two
+    copies.  A running request reads only the re-numbered one, so the other
+    can be evicted, after which a history needing the first positions must
+    restore while the running one still reuses."""
+    v0 = _hist([P_, Q_])                               # Q at positions 6..10
+    v1 = _hist([P_, Q_], drops=[(1, 0)], repos=[1])    # P dropped, Q moved to 0..4
+    tree.insert(*v0, 1)
+    tree.finish(1)
+    tree.insert(*v1, 2)                                # runs on Q's new copy
+    assert tree.evict(len(P_)) == len(P_)              # the dropped P first
+    assert tree.evict(len(Q_)) == len(Q_)              # Q's first-position copy
+    assert tree.match(*v1)["kind"] == "reuse"
+    m = tree.match(*v0)
+    assert m["kind"] == "restore" and m["restore_tokens"] == len(P_) + len(Q_)
+    assert tree.evict(10 ** 9) == 0                    # the new copy is in use
+    tree.finish(2)
+    assert tree.evict(10 ** 9) == len(Q_)
