@@ -6,6 +6,7 @@ import pytest
 import kv_cache_drop_gb300 as akv
 import oracle
 import workloads
+from _util import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -200,3 +201,79 @@ def test_decoder_full_size_properties():
     rel, mx = _rel(pref[:n], ref)
     print(f"[parity] decoder prefix rows: rel_rms={rel:.3e} max_abs={mx:.3e}")
     assert rel <= MODEL_REL_RMS and mx <= MODEL_MAX_ABS
+
+
+def _op_rows(mw, b, n_total=64, seed=0):
+    """Rows of request b next to each of its op boundaries (the last row
+    before it, the first two after it), then random rows up to n_total."""
+    _, da, _, ra = (mw.msg_start, *mw.ops[b])
+    T = mw.T
+    pick = set()
+    for a in sorted({int(x) for x in da} | {int(x) for x in ra}):
+        s = int(mw.msg_start[a + 1])
+        pick.update(t for t in (s - 1, s, s + 1) if 0 <= t < T)
+    rng = np.random.default_rng(seed + b)
+    while len(pick) < n_total:
+        pick.add(int(rng.integers(0, T)))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def test_decoder_full_size_teacher_forced_layers():
+    """Full-size decoder workload (8,192 shared + 24,576 diverging tokens),
+    requests 1, 2 and 5 (one, two and two repos): every layer's segmented
+    attention on op-bearing rows against the oracle fed the GPU's own layer
+    input.
+
+    Layer l's input: akv_decoder_forward run with the first l layers returns
+    the final RMSNorm of the residual stream after those layers, which (the
+    RMSNorm weights are 1) is layer l's normalised input.  Rounded to bf16,
+    it goes through layer l's Q/K/V projections (akv_gemm_bf16, the
+    forward's GEMM kernel) and then the segment attention over the batch's
+    plan; the oracle replays the request's op log over the same Q/K/V bytes.
+    Rows right after each drop and repos boundary are always among the
+    compared ones."""
+    from oracle.parallel import replay_attention_rows
+    torch = _torch()
+    full = workloads.model_workload()
+    reqs = [1, 2, 5]
+    assert [len(full.ops[b][2]) for b in reqs] == [1, 2, 2]
+    T, d = full.T, full.d_model
+    shp = akv.shape(full.Hq, full.Hkv, full.D, "bf16", full.rope_base)
+    ops = [(full.msg_start, *full.ops[b]) for b in reqs]
+    plan = akv.Plan(shp, np.arange(len(reqs) + 1) * T, ops)
+    x = _bf16(np.concatenate([full.x] * len(reqs)))
+    weights = _gpu_weights(full)
+    n = len(reqs) * T
+    dq, dkv = full.Hq * full.D, full.Hkv * full.D
+    ws = torch.empty(akv.akv_decoder_workspace(plan, d, full.d_ff), dtype=torch.uint8,
+                     device="cuda")
+    aws = plan.workspace()
+    h = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    worst = 0.0
+    for l in range(full.n_layers):
+        akv.akv_decoder_forward(plan, weights[:l], d, full.d_ff, full.eps, x, h, ws)
+        a = h.to(torch.bfloat16)
+        q = torch.empty((n, dq), dtype=torch.bfloat16, device="cuda")
+        k = torch.empty((n, dkv), dtype=torch.bfloat16, device="cuda")
+        v = torch.empty((n, dkv), dtype=torch.bfloat16, device="cuda")
+        akv.akv_gemm_bf16(n, dq, d, a, weights[l]["wq"], q, 0)
+        akv.akv_gemm_bf16(n, dkv, d, a, weights[l]["wk"], k, 0)
+        akv.akv_gemm_bf16(n, dkv, d, a, weights[l]["wv"], v, 0)
+        o = torch.empty_like(q)
+        akv.akv_segment_attention_run(plan, q, k, v, o, aws)
+        torch.cuda.synchronize()
+        assert akv.akv_workspace_status(aws) == 0, "a kernel barrier wait timed out"
+        qs, ks, vs, os_ = (t.view(torch.int16).cpu().numpy().view(np.uint16)
+                           for t in (q, k, v, o))
+        for i, b in enumerate(reqs):
+            sl = slice(i * T, (i + 1) * T)
+            rows = _op_rows(full, b, seed=10 * l)
+            ref = replay_attention_rows(
+                ops[i], qs[sl].reshape(T, full.Hq, full.D), ks[sl].reshape(T, full.Hkv, full.D),
+                vs[sl].reshape(T, full.Hkv, full.D), "bf16", full.rope_base, rows)
+            got = oracle.widen(os_[sl].reshape(T, full.Hq, full.D)[rows], "bf16")
+            print(f"[parity] layer {l} request {b}: {len(rows)} rows")
+            mx, _ = assert_close(got, ref, "bf16")
+            worst = max(worst, mx)
+    del weights
+    print(f"[parity] teacher-forced layers: worst max_abs {worst:.3e}")
