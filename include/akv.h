@@ -369,18 +369,28 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
  * allocate per call.  Same arguments, semantics and results as
  * akv_decode_attention, minus the workspace: the split-KV partials go to a
  * fixed array in the library's device memory,
- * akv_decode_static_scratch_bytes() bytes (16 MiB) on every GPU that loads
- * the library, held until the process exits.  Nothing is allocated by the
- * call (no cudaMalloc/cudaFree, no allocating library routine).
+ * akv_decode_static_scratch_bytes() bytes (16 MiB) on every GPU where the
+ * library's decode module is loaded (see Set-up), held until the process
+ * exits.  Nothing is allocated by the call (no cudaMalloc/cudaFree, no allocating library routine).
  *  - Limit: the bytes akv_decode_workspace() returns for the same shape, B
  *    and max_kv (split-KV partials, B * Hq * ceil(max_kv / 1024) * 66 * 4
  *    bytes, plus B * Hkv * 4 bytes of merge counters, each part rounded up
  *    to 256) must fit the array; larger requests return
  *    AKV_ERR_UNSUPPORTED with the sizes in akv_last_error(), before
  *    anything is enqueued.
- *  - Set-up: the first call on a device (with that device current) looks up
- *    the array's device address with cudaGetSymbolAddress and caches it; make
- *    that first call before any stream capture.
+ *  - Set-up: the array lives in the library module that holds the decode
+ *    kernels.  With CUDA's default lazy module loading that module (and
+ *    its 16 MiB) is loaded on a device the first time one of the decode
+ *    entry points runs there, so the reservation can fail then if the
+ *    device is already full; with CUDA_MODULE_LOADING=EAGER it is loaded
+ *    with the library.  A call with B = 0 does only this set-up (no launch;
+ *    only `shape` is read): a caller that wants the memory reserved up
+ *    front makes that call at initialisation, with the device current.
+ *    Every call looks the array's address up again (cudaGetSymbolAddress
+ *    in the current context, which allocates nothing), so a device reset or
+ *    a different context made current between calls does not leave it
+ *    writing through a stale address.  Make the first call on a device
+ *    before any stream capture.
  *  - Sharing: every call on a device uses the same array.  Calls that
  *    overlap on the GPU (other streams, other host threads) race and corrupt
  *    each other's results; serialise them.  The array keeps the last call's

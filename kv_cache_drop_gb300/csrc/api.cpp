@@ -1216,7 +1216,12 @@ akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const 
   if (akv_status st = check_shape(shape)) return st;
   if (B < 0 || max_kv < 0) return fail(AKV_ERR_INVALID, "negative size");
   if (B > 65535) return fail(AKV_ERR_UNSUPPORTED, "decode supports B <= 65535");
-  if (B == 0) return AKV_OK;
+  if (B == 0) {  // set-up only: loads the module that holds the array
+    void *scratch = nullptr;
+    const cudaError_t e = decode_static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "static decode scratch look-up");
+    return AKV_OK;
+  }
   if (!q || !q_pos || !k_pool || !v_pool || !kv_indptr || !out || (max_kv > 0 && !kv_indices))
     return fail(AKV_ERR_INVALID, "NULL argument");
   if (shape->dtype == AKV_BF16 && shape->Hq / shape->Hkv > 16)

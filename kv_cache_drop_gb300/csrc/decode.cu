@@ -20,7 +20,6 @@
 #include "common.cuh"
 
 #include <algorithm>
-#include <mutex>
 
 namespace akv {
 namespace {
@@ -913,33 +912,27 @@ cudaError_t launch_check_indices(int B, const int32_t *indptr, const int32_t *in
 }
 
 // ---------------------------------------------------------------------------
-// Decode without a caller workspace.  The split-KV partials go to a fixed
-// array in this module's device memory instead: every GPU that loads the
-// library keeps kStaticScratchBytes for it until the process exits.  Host
+// Decode without a caller workspace.  The split-KV partials and merge
+// counters go to a fixed array in this module's device memory instead: every
+// GPU on which the module is loaded keeps kStaticScratchBytes for it until the
+// process exits (under lazy module loading the module, and so the array, is
+// loaded with the first use of one of this file's kernels or symbols).  Host
 // code cannot pass the array's name to a kernel (on the host it is only a
-// stand-in, not a device address), so its address is looked up once per
-// device with cudaGetSymbolAddress and cached.
+// stand-in, not a device address), so every call looks its address up with
+// cudaGetSymbolAddress in the current context.  The address is not cached:
+// it belongs to the context the module was loaded into, and a device reset
+// or another context made current on the same device would leave a cached
+// one pointing at memory that is no longer this array.
 // ---------------------------------------------------------------------------
 namespace {
 __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 }  // namespace
 
 cudaError_t decode_static_scratch(void **ptr) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *a = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&a, g_decode_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void *a = nullptr;
-    e = cudaGetSymbolAddress(&a, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = a;
-  }
-  *ptr = addr[dev];
+  *ptr = a;
   return cudaSuccess;
 }
 
@@ -948,20 +941,10 @@ cudaError_t launch_decode_static(int dtype, int B, int Hq, int Hkv, const void *
                                  const int32_t *indptr, const int32_t *indices, int max_kv,
                                  void *out, const RopeTheta &th, cudaStream_t s) {
   void *scratch = nullptr;
-  cudaError_t e = decode_static_scratch(&scratch);
+  const cudaError_t e = decode_static_scratch(&scratch);
   if (e != cudaSuccess) return e;
-  const int ns = n_splits(max_kv);
-  Partials part = partials(scratch, B, Hq, max_kv);
-  if (dtype == AKV_BF16) {
-    return decode_bf16(B, Hq, Hkv, q, qpos, const_cast<void *>(kp), const_cast<void *>(vp),
-                       indptr, indices, max_kv, out, scratch, th, nullptr, nullptr, nullptr, s);
-  } else {
-    decode_f32_kernel<<<dim3(ns, Hq, B), 128, 0, s>>>(Hq, Hkv, (const float *)q, qpos,
-                                                      (const float *)kp, (const float *)vp,
-                                                      indptr, indices, part, th);
-    decode_combine_kernel<float><<<dim3(Hq, B), kD, 0, s>>>(Hq, ns, kChunk, indptr, part, (float *)out);
-  }
-  return cudaGetLastError();
+  return launch_decode(dtype, B, Hq, Hkv, q, qpos, kp, vp, indptr, indices, max_kv, out, scratch,
+                       th, s);
 }
 
 }  // namespace akv
