@@ -247,9 +247,40 @@ akv_status akv_compact(const akv_oplog *ops, int32_t T, int32_t upto, int32_t *a
  * akv_tree_evict: frees (marks not resident) unpinned units until `tokens`
  *   tokens are freed or none is left: dropped units first, then by the
  *   insert that last held them (oldest first), then by creation order.
- *   *freed: tokens freed.
+ *   *freed: tokens freed.  A unit's pin count is the number of running
+ *   requests whose active cache reads that copy: a reference count per
+ *   position version.
  * Errors: AKV_ERR_INVALID for NULL arguments, a bad op log or an unknown /
- * duplicate request_id. */
+ * duplicate request_id.
+ *
+ * Pool trees (drop-aware eviction over a page-size-1 KV pool; the system
+ * README: drop and repos support page size 1 only).  akv_tree_create_pool
+ * makes a tree that also hands out the n_slots token slots of a caller-owned
+ * KV pool (the [S, Hkv, D] pools of the decode entry points, S = n_slots):
+ *  - a resident unit owns one slot per token; eviction (akv_tree_evict, or
+ *    the automatic one below) puts its slots back on the free list;
+ *  - akv_tree_insert gives every unit of the history that is not resident
+ *    the lowest free slots.  When too few are free it first evicts other
+ *    unpinned units in the order above (never a unit of the history being
+ *    inserted); if that is not enough it returns AKV_ERR_WORKSPACE and
+ *    leaves the request not running, nothing allocated;
+ *  - akv_tree_request_writes lists, per token, the slots that request's
+ *    insert allocated, with the token's logical index in the history and
+ *    its position there: the caller fills each slot with K rotated at that
+ *    position and V of that token (akv_append_kv does exactly this) before
+ *    anything reads them;
+ *  - akv_tree_request_cache lists the request's active cache at the end of
+ *    its history in logical order: slot (the kv_indices of a decode),
+ *    logical index and position per token.  The listed units are pinned, so
+ *    their slots do not move while the request runs;
+ *  - akv_tree_reserve gives a running request n more slots (for its decode
+ *    appends), evicting if needed; they are freed when it finishes;
+ *  - both lists: int32 host arrays of `cap` entries, any of them NULL; all
+ *    NULL returns the count in *n only; a cap below the count is
+ *    AKV_ERR_INVALID.  Logical indices and positions are those of the
+ *    request's own history.
+ * On a tree made by akv_tree_create these calls list slot -1 and
+ * akv_tree_reserve returns AKV_ERR_INVALID. */
 typedef struct akv_tree akv_tree;
 typedef enum {
   AKV_TREE_REUSE = 0,
@@ -274,6 +305,13 @@ akv_status akv_tree_insert(akv_tree *tree, const akv_oplog *ops, const int32_t *
 akv_status akv_tree_finish(akv_tree *tree, int64_t request_id);
 akv_status akv_tree_evict(akv_tree *tree, int64_t tokens, int64_t *freed);
 akv_status akv_tree_stats(const akv_tree *tree, akv_tree_stats_t *stats);
+akv_status akv_tree_create_pool(int64_t n_slots, akv_tree **out);
+akv_status akv_tree_request_writes(const akv_tree *tree, int64_t request_id, int32_t *slots,
+                                   int32_t *logical, int32_t *pos, int64_t cap, int64_t *n);
+akv_status akv_tree_request_cache(const akv_tree *tree, int64_t request_id, int32_t *slots,
+                                  int32_t *logical, int32_t *pos, int64_t cap, int64_t *n);
+akv_status akv_tree_reserve(akv_tree *tree, int64_t request_id, int64_t n, int32_t *slots);
+akv_status akv_tree_pool_info(const akv_tree *tree, int64_t *pool_slots, int64_t *free_slots);
 
 /* ------------------------------------------------------------------------
  * Repos / position-version conversion (section 3.3, section 4.2 and

@@ -101,6 +101,17 @@ _SIGS = {
     "akv_tree_evict": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64,
                                       ctypes.POINTER(ctypes.c_int64)]),
     "akv_tree_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(TreeStats)]),
+    "akv_tree_create_pool": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)]),
+    "akv_tree_request_writes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p,
+                                               _i32p, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_int64)]),
+    "akv_tree_request_cache": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p,
+                                              _i32p, ctypes.c_int64,
+                                              ctypes.POINTER(ctypes.c_int64)]),
+    "akv_tree_reserve": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                        _i32p]),
+    "akv_tree_pool_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64)]),
     "akv_plan_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PlanInfo)]),
     "akv_plan_tables": (ctypes.c_int, [ctypes.c_void_p, _i32p, _i32p, _i32p, _i32p]),
     "akv_segment_attention_run": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 5 +
@@ -249,10 +260,15 @@ class Tree:
     is (ops, token_ids): an op log tuple as for Plan and the messages' token
     ids (int32, msg_start[-1] of them)."""
 
-    def __init__(self):
+    def __init__(self, pool_slots: int = 0):
+        """pool_slots > 0: the tree also manages the token slots of a
+        page-size-1 KV pool of that many slots (akv_tree_create_pool)."""
         self._lib = lib()
         h = ctypes.c_void_p()
-        _check(self._lib.akv_tree_create(ctypes.byref(h)))
+        if pool_slots:
+            _check(self._lib.akv_tree_create_pool(pool_slots, ctypes.byref(h)))
+        else:
+            _check(self._lib.akv_tree_create(ctypes.byref(h)))
         self.handle = h
 
     def __del__(self):
@@ -292,6 +308,34 @@ class Tree:
         st = TreeStats()
         _check(self._lib.akv_tree_stats(self.handle, ctypes.byref(st)))
         return st.as_dict()
+
+    def _list(self, fn, request_id: int):
+        n = ctypes.c_int64(0)
+        _check(fn(self.handle, request_id, None, None, None, 0, ctypes.byref(n)))
+        out = [np.empty(n.value, dtype=np.int32) for _ in range(3)]
+        _check(fn(self.handle, request_id, *[o.ctypes.data_as(_i32p) for o in out], n.value,
+                  ctypes.byref(n)))
+        return dict(slots=out[0], logical=out[1], pos=out[2])
+
+    def request_writes(self, request_id: int) -> dict:
+        """Slots the request's insert allocated: dict of int32 arrays slots,
+        logical, pos (fill slot with K rotated at pos and V of token logical)."""
+        return self._list(self._lib.akv_tree_request_writes, request_id)
+
+    def request_cache(self, request_id: int) -> dict:
+        """The request's active cache in logical order: slots, logical, pos."""
+        return self._list(self._lib.akv_tree_request_cache, request_id)
+
+    def reserve(self, request_id: int, n: int) -> np.ndarray:
+        out = np.empty(n, dtype=np.int32)
+        _check(self._lib.akv_tree_reserve(self.handle, request_id, n,
+                                          out.ctypes.data_as(_i32p)))
+        return out
+
+    def pool_info(self) -> dict:
+        a, b = ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(self._lib.akv_tree_pool_info(self.handle, ctypes.byref(a), ctypes.byref(b)))
+        return dict(pool_slots=a.value, free_slots=b.value)
 
 
 class Plan:

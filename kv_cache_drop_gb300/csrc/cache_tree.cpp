@@ -19,10 +19,20 @@
 // Storage units: a message node's own KV (at the positions it was computed
 // with), and at every repos node one re-rotated copy of each message alive
 // there (the new position version).  Each unit is resident or evicted,
-// pinned by the running requests whose active cache uses it, and marked
-// dropped when the latest request using it dropped it.
+// pinned by the running requests whose active cache uses it (the pin count
+// is the reference count of that position version), and marked dropped
+// when the latest request using it dropped it.
+//
+// Pool trees (akv_tree_create_pool) also manage the token slots of a
+// page-size-1 KV pool (the system README: drop and repos support page size 1
+// only): a resident unit owns one slot per token, eviction returns its slots
+// to the free list, an insert takes slots for the units it makes resident
+// (lowest free slots first), evicting unpinned units in the same drop-aware
+// order when the free list is short, and a running request can hold extra
+// slots for its decode appends until it finishes.
 #include <algorithm>
 #include <cstdint>
+#include <iterator>
 #include <map>
 #include <memory>
 #include <vector>
@@ -42,6 +52,8 @@ struct Unit {  // one storage unit: the KV of one message at one position versio
   int pins = 0;
   uint64_t last_use = 0;  // insert count of the latest request holding it
   uint64_t seq = 0;       // creation order (ties in eviction order)
+  bool busy = false;      // on the path of the insert in progress (not evictable by it)
+  std::vector<int32_t> slots;  // pool trees: one pool slot per token while resident
 };
 
 struct Node {
@@ -162,13 +174,86 @@ Walk walk(Node *root, const akv_oplog *o, const int32_t *tok, const std::vector<
 
 }  // namespace
 
+namespace {
+
+// A unit's tokens as they sit in one history: its first logical token and
+// the position of that token (positions inside a message are consecutive).
+struct Placed {
+  Unit *u;
+  int64_t first_logical, first_pos;
+};
+
+struct Running {
+  std::vector<Placed> active;   // newest copy of each active message, logical order (pinned)
+  std::vector<Placed> written;  // units its insert gave new slots (to be filled by the caller)
+  std::vector<int32_t> tail;    // slots held for decode appends
+};
+
+// Free slots of a pool as disjoint ranges [first, first + count), by first.
+class FreeSlots {
+ public:
+  void reset(int64_t n) {
+    r_.clear();
+    n_ = 0;
+    if (n > 0) add(0, n);
+  }
+  int64_t size() const { return n_; }
+  // the lowest n free slots
+  void take(int64_t n, std::vector<int32_t> *out) {
+    while (n > 0) {
+      auto it = r_.begin();
+      const int64_t k = std::min<int64_t>(n, it->second);
+      for (int64_t i = 0; i < k; ++i) out->push_back((int32_t)(it->first + i));
+      const int64_t first = it->first + k, left = it->second - k;
+      r_.erase(it);
+      if (left) r_.emplace(first, left);
+      n -= k;
+      n_ -= k;
+    }
+  }
+  void give(const std::vector<int32_t> &slots) {
+    std::vector<int32_t> s(slots);
+    std::sort(s.begin(), s.end());
+    for (size_t i = 0; i < s.size();) {
+      size_t j = i + 1;
+      while (j < s.size() && s[j] == s[j - 1] + 1) ++j;
+      add(s[i], (int64_t)(j - i));
+      i = j;
+    }
+  }
+
+ private:
+  void add(int64_t first, int64_t count) {
+    n_ += count;
+    auto next = r_.lower_bound(first);
+    if (next != r_.end() && next->first == first + count) {  // join the range after
+      count += next->second;
+      next = r_.erase(next);
+    }
+    if (next != r_.begin()) {
+      auto prev = std::prev(next);
+      if (prev->first + prev->second == first) {  // join the range before
+        prev->second += count;
+        return;
+      }
+    }
+    r_.emplace(first, count);
+  }
+  std::map<int64_t, int64_t> r_;
+  int64_t n_ = 0;
+};
+
+}  // namespace
+
 struct akv_tree {
   Node root;
   uint64_t tick = 0;
   uint64_t units = 0;  // storage units created
   int64_t n_nodes = 1;
-  // running requests: the units each one pins
-  std::map<int64_t, std::vector<Unit *>> running;
+  int64_t pool = 0;    // slots of the managed KV pool (0: no pool)
+  FreeSlots free;
+  // running requests: what each one pins, was given and holds
+  std::map<int64_t, Running> running;
 };
 
 namespace {
@@ -194,6 +279,60 @@ void copies_of(const Walk &w, const Replay &r, int j, std::vector<std::pair<int,
   }
 }
 
+// Free unpinned resident units (not on the path of an insert in progress)
+// until `tokens` tokens are freed or none is left: dropped units first, then
+// the rest, least recently used first within each class, then by creation.
+// Nodes stay as empty placeholders; a pool tree gets the units' slots back.
+int64_t evict_units(akv_tree *t, int64_t tokens) {
+  std::vector<Unit *> cand;
+  std::vector<Node *> stack{&t->root};
+  while (!stack.empty()) {
+    Node *nd = stack.back();
+    stack.pop_back();
+    if (nd->kind == Node::kMsg && nd->own.resident && nd->own.pins == 0 && !nd->own.busy)
+      cand.push_back(&nd->own);
+    for (auto &kv : nd->ver)
+      if (kv.second.resident && kv.second.pins == 0 && !kv.second.busy) cand.push_back(&kv.second);
+    for (auto &c : nd->children) stack.push_back(c.get());
+  }
+  std::sort(cand.begin(), cand.end(), [](const Unit *a, const Unit *b) {
+    if (a->dropped != b->dropped) return a->dropped;
+    if (a->last_use != b->last_use) return a->last_use < b->last_use;
+    return a->seq < b->seq;
+  });
+  int64_t freed = 0;
+  for (Unit *u : cand) {
+    if (freed >= tokens) break;
+    u->resident = false;  // the node stays as an empty placeholder
+    freed += u->tokens;
+    if (t->pool) {
+      t->free.give(u->slots);
+      u->slots.clear();
+    }
+  }
+  return freed;
+}
+
+// Copy a list of placed units' slots, logical indices and positions out.
+akv_status list_out(const std::vector<Placed> &list, int32_t *slots, int32_t *logical,
+                    int32_t *pos, int64_t cap, int64_t *n) {
+  int64_t total = 0;
+  for (const Placed &p : list) total += p.u->tokens;
+  *n = total;
+  if (!slots && !logical && !pos) return AKV_OK;  // size query
+  if (cap < total)
+    return report_error(AKV_ERR_INVALID, "capacity %lld < %lld entries", (long long)cap,
+                        (long long)total);
+  int64_t k = 0;
+  for (const Placed &p : list)
+    for (int64_t i = 0; i < p.u->tokens; ++i, ++k) {
+      if (slots) slots[k] = p.u->slots.empty() ? -1 : p.u->slots[i];
+      if (logical) logical[k] = (int32_t)(p.first_logical + i);
+      if (pos) pos[k] = (int32_t)(p.first_pos + i);
+    }
+  return AKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,6 +341,16 @@ akv_status akv_tree_create(akv_tree **out) {
   if (!out) return report_error(AKV_ERR_INVALID, "out is NULL");
   *out = new (std::nothrow) akv_tree;
   if (!*out) return report_error(AKV_ERR_INVALID, "host allocation failed");
+  return AKV_OK;
+}
+
+akv_status akv_tree_create_pool(int64_t n_slots, akv_tree **out) {
+  if (!out) return report_error(AKV_ERR_INVALID, "out is NULL");
+  if (n_slots <= 0 || n_slots > INT32_MAX)
+    return report_error(AKV_ERR_INVALID, "pool slots must be in 1..2^31-1");
+  if (akv_status st = akv_tree_create(out)) return st;
+  (*out)->pool = n_slots;
+  (*out)->free.reset(n_slots);
   return AKV_OK;
 }
 
@@ -294,11 +443,12 @@ akv_status akv_tree_insert(akv_tree *t, const akv_oplog *ops, const int32_t *tok
       cur = on;
     }
   }
+  // every unit the history makes resident, in the order they are created:
+  // each message's own KV, and at each repos a copy of every message alive
+  std::vector<Placed> path;
   std::vector<char> alive(n, 0);
   for (int m = 0; m < n; ++m) {
-    Unit &u = msg[m]->own;
-    u.resident = true;
-    u.last_use = now;
+    path.push_back({&msg[m]->own, ops->msg_start[m], r.first_pos[r.ver_of[m]][m]});
     alive[m] = 1;
     for (int j : os[m].drops) alive[j] = 0;
     if (repos[m])
@@ -308,14 +458,45 @@ akv_status akv_tree_insert(akv_tree *t, const akv_oplog *ops, const int32_t *tok
           Unit &c = ins.first->second;
           if (ins.second) c.seq = ++t->units;
           c.tokens = ops->msg_start[j + 1] - ops->msg_start[j];
-          c.resident = true;
-          c.last_use = now;
+          path.push_back({&c, ops->msg_start[j], r.first_pos[r.ver_of[m] + 1][j]});
         }
+  }
+  // pool: slots for the units that are not resident yet, evicting other
+  // unpinned units (drop-aware order) when the free list is short
+  std::vector<Placed> written;
+  if (t->pool) {
+    // every unit sits on the path once (one per message node, one per
+    // message node and repos node)
+    int64_t need = 0;
+    for (Placed &p : path) {
+      p.u->busy = true;
+      if (!p.u->resident) need += p.u->tokens;
+    }
+    if (t->free.size() < need) evict_units(t, need - t->free.size());
+    if (t->free.size() < need) {
+      for (Placed &p : path) p.u->busy = false;
+      return report_error(AKV_ERR_WORKSPACE,
+                          "KV pool full: %lld slots needed, %lld free after evicting every "
+                          "unpinned unit", (long long)need, (long long)t->free.size());
+    }
+    for (Placed &p : path) {
+      p.u->busy = false;
+      if (!p.u->resident) {
+        t->free.take(p.u->tokens, &p.u->slots);
+        written.push_back(p);
+      }
+    }
+  }
+  for (Placed &p : path) {
+    p.u->resident = true;
+    p.u->last_use = now;
   }
   // the request's active cache at the end: the newest copy of each message
   // still alive is pinned; the rest of its path is marked by whether this
   // (latest) user dropped it
-  std::vector<Unit *> &pins = t->running[request_id];
+  Running &run = t->running[request_id];
+  run.written = std::move(written);
+  const int vfin = r.n_ver - 1;
   for (int j = 0; j < n; ++j) {
     Unit *newest = &msg[j]->own;  // the copy at the last version holding it
     for (int m = j; m < n; ++m)
@@ -332,7 +513,7 @@ akv_status akv_tree_insert(akv_tree *t, const akv_oplog *ops, const int32_t *tok
       }
     if (act) {
       ++newest->pins;
-      pins.push_back(newest);
+      run.active.push_back({newest, ops->msg_start[j], r.first_pos[vfin][j]});
     }
   }
   return AKV_OK;
@@ -343,36 +524,57 @@ akv_status akv_tree_finish(akv_tree *t, int64_t request_id) {
   auto it = t->running.find(request_id);
   if (it == t->running.end())
     return report_error(AKV_ERR_INVALID, "request %lld is not running", (long long)request_id);
-  for (Unit *u : it->second) --u->pins;
+  for (Placed &p : it->second.active) --p.u->pins;
+  if (t->pool) t->free.give(it->second.tail);
   t->running.erase(it);
   return AKV_OK;
 }
 
 akv_status akv_tree_evict(akv_tree *t, int64_t tokens, int64_t *freed) {
   if (!t || !freed) return report_error(AKV_ERR_INVALID, "NULL argument");
-  *freed = 0;
-  // candidates: resident, pinned by no running request; dropped ones first,
-  // then the rest, least recently used first within each class
-  std::vector<Unit *> cand;
-  std::vector<Node *> stack{&t->root};
-  while (!stack.empty()) {
-    Node *nd = stack.back();
-    stack.pop_back();
-    if (nd->kind == Node::kMsg && nd->own.resident && nd->own.pins == 0) cand.push_back(&nd->own);
-    for (auto &kv : nd->ver)
-      if (kv.second.resident && kv.second.pins == 0) cand.push_back(&kv.second);
-    for (auto &c : nd->children) stack.push_back(c.get());
-  }
-  std::sort(cand.begin(), cand.end(), [](const Unit *a, const Unit *b) {
-    if (a->dropped != b->dropped) return a->dropped;
-    if (a->last_use != b->last_use) return a->last_use < b->last_use;
-    return a->seq < b->seq;
-  });
-  for (Unit *u : cand) {
-    if (*freed >= tokens) break;
-    u->resident = false;  // the node stays as an empty placeholder
-    *freed += u->tokens;
-  }
+  *freed = evict_units(t, tokens);
+  return AKV_OK;
+}
+
+akv_status akv_tree_request_cache(const akv_tree *t, int64_t request_id, int32_t *slots,
+                                  int32_t *logical, int32_t *pos, int64_t cap, int64_t *n) {
+  if (!t || !n) return report_error(AKV_ERR_INVALID, "NULL argument");
+  auto it = t->running.find(request_id);
+  if (it == t->running.end())
+    return report_error(AKV_ERR_INVALID, "request %lld is not running", (long long)request_id);
+  return list_out(it->second.active, slots, logical, pos, cap, n);
+}
+
+akv_status akv_tree_request_writes(const akv_tree *t, int64_t request_id, int32_t *slots,
+                                   int32_t *logical, int32_t *pos, int64_t cap, int64_t *n) {
+  if (!t || !n) return report_error(AKV_ERR_INVALID, "NULL argument");
+  auto it = t->running.find(request_id);
+  if (it == t->running.end())
+    return report_error(AKV_ERR_INVALID, "request %lld is not running", (long long)request_id);
+  return list_out(it->second.written, slots, logical, pos, cap, n);
+}
+
+akv_status akv_tree_reserve(akv_tree *t, int64_t request_id, int64_t n, int32_t *slots) {
+  if (!t || (n > 0 && !slots) || n < 0) return report_error(AKV_ERR_INVALID, "bad argument");
+  if (!t->pool) return report_error(AKV_ERR_INVALID, "the tree manages no pool");
+  auto it = t->running.find(request_id);
+  if (it == t->running.end())
+    return report_error(AKV_ERR_INVALID, "request %lld is not running", (long long)request_id);
+  if (t->free.size() < n) evict_units(t, n - t->free.size());
+  if (t->free.size() < n)
+    return report_error(AKV_ERR_WORKSPACE, "KV pool full: %lld slots asked, %lld free",
+                        (long long)n, (long long)t->free.size());
+  std::vector<int32_t> got;
+  t->free.take(n, &got);
+  std::copy(got.begin(), got.end(), slots);
+  it->second.tail.insert(it->second.tail.end(), got.begin(), got.end());
+  return AKV_OK;
+}
+
+akv_status akv_tree_pool_info(const akv_tree *t, int64_t *pool_slots, int64_t *free_slots) {
+  if (!t || !pool_slots || !free_slots) return report_error(AKV_ERR_INVALID, "NULL argument");
+  *pool_slots = t->pool;
+  *free_slots = t->pool ? t->free.size() : 0;
   return AKV_OK;
 }
 

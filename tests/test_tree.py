@@ -262,3 +262,132 @@ def test_position_versions_evicted_separately(tree):
     assert tree.evict(10 ** 9) == 0                    # the new copy is in use
     tree.finish(2)
     assert tree.evict(10 ** 9) == len(Q_)
+
+
+# --- pool trees: the tree hands out the slots of a page-size-1 KV pool
+
+
+def test_pool_cache_lists_match_replay(akv):
+    """For random histories, the active cache a pool tree lists for a running
+    request is the oracle replay's active cache: the same logical tokens at
+    the same positions, in logical order; every slot is distinct and in the
+    pool, and a fresh insert's writes cover every token of its history
+    (each message once, plus one copy per survivor at each repos)."""
+    import oracle
+    rng = np.random.default_rng(5)
+    for i in range(40):
+        ops, tok = _random_history(rng)
+        ms = ops[0]
+        t = akv.Tree(pool_slots=4096)
+        t.insert(ops, tok, 1)
+        c = t.request_cache(1)
+        rep = oracle.replay(*ops)
+        np.testing.assert_array_equal(c["logical"], rep.active_u)
+        np.testing.assert_array_equal(c["pos"], rep.active_p)
+        assert len(set(c["slots"].tolist())) == len(c["slots"])
+        assert ((c["slots"] >= 0) & (c["slots"] < 4096)).all()
+        w = t.request_writes(1)
+        n_copies = 0
+        for a in sorted({int(x) for x in ops[3]}):
+            n_copies += len(oracle.compact(*ops, upto=a)[0])
+        assert len(w["slots"]) == int(ms[-1]) + n_copies
+        assert len(set(w["slots"].tolist())) == len(w["slots"])
+        # the listed cache slots are among the written ones, holding the same
+        # token at the same position
+        wmap = {int(s): (int(u), int(p)) for s, u, p in zip(w["slots"], w["logical"], w["pos"])}
+        for s, u, p in zip(c["slots"], c["logical"], c["pos"]):
+            assert wmap[int(s)] == (int(u), int(p))
+
+
+def test_pool_insert_takes_the_dropped_slots_first(akv):
+    """A full pool: the next insert evicts, in the drop-aware order, just the
+    dropped message, and its tokens land in exactly the slots it freed."""
+    done = _hist([R_, S_])
+    dropped = _hist([P_, Q_], drops=[(1, 0)])
+    S = len(R_) + len(S_) + len(P_) + len(Q_)
+    t = akv.Tree(pool_slots=S)
+    t.insert(*done, 1)
+    t.finish(1)
+    t.insert(*dropped, 2)
+    w = t.request_writes(2)
+    p_slots = sorted(int(s) for s, u in zip(w["slots"], w["logical"]) if u < len(P_))
+    t.finish(2)
+    assert t.pool_info() == {"pool_slots": S, "free_slots": 0}
+    X = [15] * len(P_)
+    t.insert(*_hist([X]), 3)
+    assert sorted(t.request_writes(3)["slots"].tolist()) == p_slots
+    assert t.match(*done)["kind"] == "reuse" and t.match(*dropped)["kind"] == "reuse"
+    assert t.match(*_hist([P_]))["kind"] == "restore"
+
+
+def test_pool_full_of_pinned_units_refuses(akv):
+    """Every slot read by a running request: an insert that needs more
+    fails, frees nothing and leaves that request not running; a reserve
+    beyond the free slots fails the same way."""
+    h = _hist([P_, Q_])
+    t = akv.Tree(pool_slots=len(P_) + len(Q_) + 2)
+    t.insert(*h, 1)
+    with pytest.raises(akv.AkvError) as e:
+        t.insert(*_hist([R_]), 2)
+    assert e.value.status == 3
+    assert t.pool_info()["free_slots"] == 2 and t.stats()["running"] == 1
+    with pytest.raises(akv.AkvError):
+        t.finish(2)
+    tail = t.reserve(1, 2)
+    assert sorted(tail.tolist()) == [len(P_) + len(Q_), len(P_) + len(Q_) + 1]
+    with pytest.raises(akv.AkvError):
+        t.reserve(1, 1)
+    t.finish(1)  # the tail comes back; the units stay resident until evicted
+    assert t.pool_info()["free_slots"] == 2
+    assert t.evict(10 ** 9) == len(P_) + len(Q_)
+    assert t.pool_info()["free_slots"] == len(P_) + len(Q_) + 2
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_pool_random_operations_keep_slots_consistent(akv, seed):
+    """Random inserts, finishes, evictions and reserves on a small pool:
+    resident tokens + held tails + free slots always add up to the pool; a
+    slot listed by several running requests holds the same token at the
+    same position for each; tails never overlap a listed slot; an insert
+    that cannot get slots fails without changing the pool."""
+    rng = np.random.default_rng(100 + seed)
+    hist = [_random_history(rng, max_msgs=6) for _ in range(16)]
+    S = 48
+    t = akv.Tree(pool_slots=S)
+    running, tails, rid = {}, {}, 0
+    for step in range(300):
+        op = rng.random()
+        if op < 0.45:
+            rid += 1
+            before = t.pool_info()["free_slots"]
+            try:
+                t.insert(*hist[int(rng.integers(len(hist)))], rid)
+                running[rid] = True
+                tails[rid] = []
+            except akv.AkvError as e:
+                assert e.status == 3
+                assert t.pool_info()["free_slots"] >= before  # evictions only
+        elif op < 0.7 and running:
+            r = list(running)[int(rng.integers(len(running)))]
+            t.finish(r)
+            del running[r], tails[r]
+        elif op < 0.85 and running:
+            r = list(running)[int(rng.integers(len(running)))]
+            try:
+                tails[r] += t.reserve(r, int(rng.integers(1, 4))).tolist()
+            except akv.AkvError as e:
+                assert e.status == 3
+        else:
+            t.evict(int(rng.integers(1, 20)))
+        info, st = t.pool_info(), t.stats()
+        held = sum(len(v) for v in tails.values())
+        assert st["resident_tokens"] + held + info["free_slots"] == S, step
+        owner = {}
+        for r in running:
+            c = t.request_cache(r)
+            for s, u, p in zip(c["slots"].tolist(), c["logical"].tolist(), c["pos"].tolist()):
+                assert 0 <= s < S
+                assert owner.setdefault(s, (u, p)) == (u, p), step
+        all_tails = [s for v in tails.values() for s in v]
+        assert len(set(all_tails)) == len(all_tails)
+        assert not set(all_tails) & set(owner), step
