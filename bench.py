@@ -599,6 +599,51 @@ def cpu_baseline(traj, seconds: float, seed: int = 0, pool=None):
                 seconds=wall)
 
 
+def oracle_configs(t3, dw, mw, seconds: float = 5.0):
+    """The oracle, as it stands, timed on a bounded sample of each of the
+    other workloads (the rolling-drop trajectory is cpu_baseline): the tiny
+    fp32 request whole; rows of the 128k repos trajectory over one worker
+    process per core; one decode step of two of the 14 requests; the
+    decoder's first 1,024 (op-free) rows.  The single-process parts run in a
+    spawned worker with one numpy thread, so their core count is 1."""
+    import oracle
+    import workloads
+    from oracle.parallel import RowPool, timed_call
+    res = {}
+    r1 = workloads.tiny_config()
+    _, sec = timed_call("oracle.core:replay_attention", dict(q=r1.q, k=r1.k, v=r1.v),
+                        msg_start=r1.msg_start, drop_after=r1.drop_after,
+                        drop_target=r1.drop_target, repos_after=r1.repos_after, dtype="f32",
+                        base=r1.rope_base)
+    res["tiny_fp32"] = dict(seconds=sec, rows=r1.T, cores=1, sample="every row")
+    vis = oracle.visible_counts(*t3.ops())
+    with RowPool(t3.q, t3.k, t3.v) as pool:
+        rows, wall, used = pool.timed(t3.ops(), t3.dtype, t3.rope_base, seconds, seed=3)
+    res["repos_128k"] = dict(tflops=float(vis[rows].sum()) * 4 * 64 * t3.Hq / wall / 1e12,
+                             rows=len(rows), seconds=wall, cores=used,
+                             sample=f"{len(rows)} random query rows x {t3.Hq} heads")
+    indptr, idx = dw.indices_at(0)
+    nb = 2
+    ip = np.asarray(indptr[:nb + 1], np.int32)
+    ix = np.asarray(idx[:ip[-1]], np.int32)
+    _, sec = timed_call("oracle.core:decode_attention",
+                        dict(q=dw.q[0][:nb], k_pool=dw.k_pool, v_pool=dw.v_pool),
+                        q_pos=(dw.L[:nb]).astype(np.int64), kv_indptr=ip, kv_indices=ix,
+                        dtype="bf16", base=10000.0)
+    nbytes = float(ip[-1]) * (2 * dw.Hkv * 64 * 2 + 4)
+    res["decode_14req"] = dict(gbs=nbytes / sec / 1e9, seconds=sec, cores=1,
+                               sample=f"step 0 of requests 0-{nb - 1} ({int(ip[-1])} active "
+                                      f"entries)")
+    n = 1024
+    _, sec = timed_call("oracle.model:model_replay", dict(x=mw.x[:n]), weights=mw.weights,
+                        msg_start=np.array([0, n], np.int32), drop_after=[], drop_target=[],
+                        repos_after=[], Hq=mw.Hq, Hkv=mw.Hkv, D=mw.D, base=mw.rope_base,
+                        eps=mw.eps)
+    res["decoder_4layer"] = dict(tokens_per_s=n / sec, seconds=sec, cores=1,
+                                 sample=f"the first {n} rows of one request, 4 layers")
+    return res
+
+
 def tree_part(agents=14, rounds=100, seed=21):
     """Host cost of the cache-history tree in an agent-serving loop: every
     round each agent's history grows by an assistant and a tool message
@@ -704,7 +749,6 @@ def run_ours(args, rank, world):
         rp["frac_of_measured_hbm"] = rp["rotate_gbs"] / pk["hbm"]
         rp["frac_of_8tbs"] = rp["rotate_gbs"] / 8000.0
         parts["repos_rotate_compact_128k"] = rp
-        del t3
         dw = workloads.decode_workload()
         rb = repos_batch_part(dw, max(5, steps), 2)
         rb["frac_of_measured_hbm"] = rb["gbs"] / pk["hbm"]
@@ -713,8 +757,8 @@ def run_ours(args, rank, world):
         dp["frac_of_measured_hbm"] = dp["gbs"] / pk["hbm"]
         dp["frac_of_8tbs"] = dp["gbs"] / 8000.0
         parts["decode_14req_256steps"] = dp
-        del dw
-        dec = decoder_part(workloads.model_workload())
+        mw = workloads.model_workload()
+        dec = decoder_part(mw)
         # both timed alone in back-to-back launches of tens of ms: burst peak
         dec["attn_frac_of_measured_burst"] = dec["attn_tflops"] / pk["bf16"]
         dec["attn_frac_of_measured_sustained"] = dec["attn_tflops"] / pk["bf16_sus"]
@@ -722,6 +766,9 @@ def run_ours(args, rank, world):
         dec["ffn_gemm_frac_of_measured_sustained"] = dec["ffn_gemm_tflops"] / pk["bf16_sus"]
         parts["decoder_4layer_32req"] = dec
         parts["cache_tree_14agents"] = tree_part()
+        if rank == 0 and not args.no_cpu:
+            parts["oracle_per_workload"] = oracle_configs(t3, dw, mw)
+        del t3, dw, mw
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup,

@@ -135,3 +135,42 @@ def timed_rows(ops, q, k, v, dtype, base, seconds, workers=None, batch=4, seed=0
     """``RowPool.timed`` on a pool made for this call."""
     with RowPool(q, k, v, workers) as pool:
         return pool.timed(ops, dtype, base, seconds, batch=batch, seed=seed)
+
+
+def _call_job(d, names, fn_path, kwargs):
+    import importlib
+    mod, fn = fn_path.split(":")
+    f = getattr(importlib.import_module(mod), fn)
+    arrays = {n: np.load(os.path.join(d, n + ".npy"), mmap_mode="r") for n in names}
+    t0 = time.perf_counter()
+    out = f(**arrays, **kwargs)
+    return out, time.perf_counter() - t0
+
+
+def timed_call(fn_path, arrays, **kwargs):
+    """Run ``fn(**arrays, **kwargs)`` (``fn_path`` = "module:function" of this
+    package) in one spawned worker with one numpy thread, the arrays passed as
+    mapped ``.npy`` files.  Returns (result, seconds the call took in the
+    worker)."""
+    d = tempfile.mkdtemp(prefix="akv_oracle_")
+    try:
+        for name, a in arrays.items():
+            np.save(os.path.join(d, name + ".npy"), np.ascontiguousarray(a))
+        saved = {n: os.environ.get(n) for n in _THREAD_VARS}
+        for n in _THREAD_VARS:
+            os.environ[n] = "1"
+        try:
+            ex = cf.ProcessPoolExecutor(1, mp_context=mp.get_context("spawn"))
+            fut = ex.submit(_call_job, d, list(arrays), fn_path, kwargs)
+        finally:
+            for n, val in saved.items():
+                if val is None:
+                    os.environ.pop(n, None)
+                else:
+                    os.environ[n] = val
+        try:
+            return fut.result()
+        finally:
+            ex.shutdown()
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
