@@ -138,6 +138,23 @@ __device__ __forceinline__ void rope_cs_fast(float hi, float lo, int pos, float 
   __sincosf(rope_angle(hi, lo, pos), s, c);
 }
 
+// cos/sin of pos * theta for frequencies f and f + 1 computed from the
+// angle itself: keys kDeltas or more positions past their tile's first one,
+// and positions beyond 2^18 (the double-precision path).  Rare, so kept out
+// of line: the unrolled loop around its call stays small.
+__device__ __noinline__ float4 rope_cs_direct2(const ThetaSmem &ts, const double *thd, int f,
+                                               int pos) {
+  float4 r;
+  if (pos < -262144 || pos > 262144) {
+    rope_cs(thd[f], (double)pos, &r.x, &r.y);
+    rope_cs(thd[f + 1], (double)pos, &r.z, &r.w);
+  } else {
+    rope_cs_fast(ts.hi[f], ts.lo[f], pos, &r.x, &r.y);
+    rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &r.z, &r.w);
+  }
+  return r;
+}
+
 template <bool kRope>
 __global__ void __launch_bounds__(kWarps * 32, 4)
     decode_bf16_kernel(int Hq, int Hkv, const __nv_bfloat16 *__restrict__ q,
@@ -153,6 +170,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   __shared__ float cs[kD / 2], sn[kD / 2];
   __shared__ ThetaSmem ts;
   __shared__ float4 dtab[kRope ? kDeltas * kDeltaRow : 1];
+  __shared__ double thd[kRope ? kD / 2 : 1];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int ns = gridDim.x;
   const int grp = Hq / Hkv;
@@ -170,6 +188,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   if (threadIdx.x < kD / 2) rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
   if (kRope) {
     stage_theta(th, ts);
+    if (threadIdx.x < kD / 2) thd[threadIdx.x] = th.th[threadIdx.x];
     // delta table: thread = (frequency f, block of 16 deltas); the block's
     // first entry directly, then 15 steps of the delta = 1 rotation
     for (int u = threadIdx.x; u < (kD / 2) * (kDeltas / 16); u += blockDim.x) {
@@ -366,12 +385,12 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
             s0f = sb0 * t.x + cb0 * t.y;
             c1f = cb1 * t.z - sb1 * t.w;
             s1f = sb1 * t.z + cb1 * t.w;
-          } else if (pos < -262144 || pos > 262144) {
-            rope_cs(th.th[f], (double)pos, &c0f, &s0f);
-            rope_cs(th.th[f + 1], (double)pos, &c1f, &s1f);
           } else {
-            rope_cs_fast(ts.hi[f], ts.lo[f], pos, &c0f, &s0f);
-            rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &c1f, &s1f);
+            const float4 d = rope_cs_direct2(ts, thd, f, pos);
+            c0f = d.x;
+            s0f = d.y;
+            c1f = d.z;
+            s1f = d.w;
           }
           __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
           __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
