@@ -184,7 +184,7 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
             ev[s][0].record(stream)
             akv.akv_segment_prepare(plan, q, k, v, ws)
             ev[s][1].record(stream)
-            akv.akv_segment_attend(plan, out, ws)
+            akv.akv_segment_attend(plan, q, out, ws)
             ev[s][2].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_start
@@ -224,6 +224,14 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        # the compute stream's own interval per step, to tell a slower kernel
+        # (copies competing for HBM and L2) from idle gaps between kernels
+        c_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(e_steps)]
+        i_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(e_steps)]
+        o_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(e_steps)]
         for it in range(-1, e_steps):  # it = -1: untimed warm-up step
             bi = it % 2
             bf = bufs[bi]
@@ -232,18 +240,30 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
                 e0.record(s_in)
             with torch.cuda.stream(s_in):
                 s_in.wait_event(computed[bi])  # step it-2 has read these inputs
+                if it >= 0:
+                    i_ev[it][0].record(s_in)
                 bf["q"].copy_(hq, non_blocking=True)
                 bf["k"].copy_(hk, non_blocking=True)
                 bf["v"].copy_(hv, non_blocking=True)
+                if it >= 0:
+                    i_ev[it][1].record(s_in)
                 in_ready[bi].record(s_in)
             s_cmp.wait_event(in_ready[bi])
             s_cmp.wait_event(out_done[bi])  # step it-2's output has left
+            if it >= 0:
+                c_ev[it][0].record(s_cmp)
             akv.akv_segment_attention(shp, cu, None, ops, bf["q"], bf["k"], bf["v"], bf["o"],
                                       bf["ws"], stream=s_cmp)
+            if it >= 0:
+                c_ev[it][1].record(s_cmp)
             computed[bi].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(computed[bi])
+                if it >= 0:
+                    o_ev[it][0].record(s_out)
                 ho[bi].copy_(bf["o"], non_blocking=True)
+                if it >= 0:
+                    o_ev[it][1].record(s_out)
                 out_done[bi].record(s_out)
         s_in.wait_stream(s_out)
         s_in.wait_stream(s_cmp)
@@ -251,6 +271,9 @@ def prefill_part(traj, steps, warmup, world, with_e2e=True):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e_steps
         res["e2e_ms"] = e2e_ms
+        res["e2e_compute_ms"] = float(np.mean([a.elapsed_time(b) for a, b in c_ev]))
+        res["e2e_h2d_ms"] = float(np.mean([a.elapsed_time(b) for a, b in i_ev]))
+        res["e2e_d2h_ms"] = float(np.mean([a.elapsed_time(b) for a, b in o_ev]))
         res["h2d_bytes"] = int(q.numel() + k.numel() + v.numel()) * q.element_size()
         res["d2h_bytes"] = int(q.numel()) * q.element_size()
         res["e2e_check"] = float((ho[(e_steps - 1) % 2].to(out.device).float() - out.float()).abs().max())
@@ -552,7 +575,7 @@ def decoder_part(mw, steps=3):
     o = torch.empty_like(q)
     aws = plan.workspace()
     akv.akv_segment_prepare(plan, q, k, v, aws)
-    attn_ms = timed(lambda: akv.akv_segment_attend(plan, o, aws), steps)
+    attn_ms = timed(lambda: akv.akv_segment_attend(plan, q, o, aws), steps)
     del q, k, v, o, aws
     a = torch.randn((T, mw.d_model), device="cuda").to(torch.bfloat16)
     g = torch.empty((T, mw.d_ff), dtype=torch.bfloat16, device="cuda")
@@ -798,6 +821,9 @@ def run_ours(args, rank, world):
             "h2d_bytes_per_step": main["h2d_bytes"], "d2h_bytes_per_step": main["d2h_bytes"],
             "ms_per_step": round(main["e2e_ms"], 3),
             "max_abs_vs_device_run": main["e2e_check"],
+            "compute_stream_ms_per_step": round(main["e2e_compute_ms"], 3),
+            "h2d_ms_per_step": round(main["e2e_h2d_ms"], 3),
+            "d2h_ms_per_step": round(main["e2e_d2h_ms"], 3),
             "note": "every step: pinned host Q/K/V -> device, akv_segment_attention (host "
                     "planning included), output -> pinned host; copies on their own streams "
                     "with two device buffer sets, so step s+1's inputs and step s-1's output "

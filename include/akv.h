@@ -165,12 +165,16 @@ akv_status akv_segment_attention_run(const akv_plan *plan, const void *q, const 
 
 /* The two halves of a run, for callers that time or overlap them:
  * akv_segment_prepare uploads the plan tables and writes the rotated and
- * permuted copies (the per-segment temporary KV versions of Appendix A.1.1)
- * into the workspace; akv_segment_attend then runs the attention over them.
- * prepare + attend on one stream == run. */
+ * permuted key and value copies (the per-segment temporary KV versions of
+ * Appendix A.1.1) into the workspace, with, for bf16, the cos/sin of every
+ * query row's angles (fp32: the rotated queries); akv_segment_attend then
+ * runs the attention over them.  For bf16 the attention kernel rotates each
+ * query row as it loads it, so attend reads q (the same raw queries as
+ * prepare; ignored for fp32, may be NULL there).  prepare + attend on one
+ * stream == run. */
 akv_status akv_segment_prepare(const akv_plan *plan, const void *q, const void *k, const void *v,
                                void *workspace, size_t workspace_bytes, akv_stream_t stream);
-akv_status akv_segment_attend(const akv_plan *plan, void *out, void *workspace,
+akv_status akv_segment_attend(const akv_plan *plan, const void *q, void *out, void *workspace,
                               size_t workspace_bytes, akv_stream_t stream);
 
 /* One-shot form: plan, then run.  Same arguments as the two calls above. */

@@ -118,7 +118,7 @@ _SIGS = {
                                   [ctypes.c_size_t, ctypes.c_void_p]),
     "akv_segment_prepare": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_size_t,
                                                                    ctypes.c_void_p]),
-    "akv_segment_attend": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_size_t,
+    "akv_segment_attend": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_size_t,
                                                                   ctypes.c_void_p]),
     "akv_segment_attention_workspace": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int32,
                                                           _i32p, ctypes.POINTER(OpLog)]),
@@ -399,8 +399,9 @@ def akv_segment_prepare(plan: Plan, q, k, v, workspace, stream=None):
                                      workspace.numel(), _stream(stream)))
 
 
-def akv_segment_attend(plan: Plan, out, workspace, stream=None):
-    _check(lib().akv_segment_attend(plan.handle, _dev(out), _dev(workspace), workspace.numel(),
+def akv_segment_attend(plan: Plan, q, out, workspace, stream=None):
+    _check(lib().akv_segment_attend(plan.handle, _dev(q), _dev(out), _dev(workspace),
+                                    workspace.numel(),
                                     _stream(stream)))
 
 

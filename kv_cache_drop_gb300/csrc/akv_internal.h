@@ -59,7 +59,9 @@ struct PlanDev {
   const MaskWin *mwin;       // [n_mask] partial windows, in tile then window order
   uint4 *mask;               // [n_mask][128 rows] visibility bits (words = keys 0-31, ..)
   const int32_t *order;      // [n_qtiles] tiles by decreasing window count
-  void *qr;                  // [Hq][T][D]  rotated queries, head-major (fp16 for bf16 inputs)
+  void *qr;                  // fp32: [Hq][T][D] rotated queries, head-major (bf16: unused)
+  float2 *qcs;               // bf16: [T][D/2] cos/sin of each row's query angles
+  const void *q;             // bf16: the raw queries [T][Hq][D] (set for the attention)
   void *kr;                  // [max_ver][Hkv][T][D] rotated keys, permuted slots, head-major
                              // (fp16 for bf16 inputs)
   void *vp;                  // [Hkv][T][D] values, permuted slots, head-major

@@ -141,7 +141,7 @@ void akv::rope_theta(float base, RopeTheta *out) {
 
 struct WsLayout {
   size_t status, tok_qpos, tok_seg, slot_src, slot_u, slot_dseg, slot_pos, qtiles, windows, mwin, mask,
-      order, qr, kr, vp, total;
+      order, qcs, qr, kr, vp, total;
 };
 
 struct akv_plan {
@@ -346,7 +346,11 @@ void layout_workspace(akv_plan *P) {
   w.mwin = take(sizeof(MaskWin) * P->mwin.size(), 256);
   w.mask = take((size_t)kTileQ * 16 * P->mwin.size(), 256);
   w.order = take(4 * nt, 256);
-  w.qr = take(es * T * P->shape.Hq * kD, 1024);
+  // bf16: the attention kernel rotates each query row itself, from the raw
+  // Q and a per-row cos/sin table; fp32: the pre-pass writes rotated queries
+  const bool bf16 = P->shape.dtype == AKV_BF16;
+  w.qcs = take(bf16 ? 8 * T * (kD / 2) : 0, 256);
+  w.qr = take(bf16 ? 0 : es * T * P->shape.Hq * kD, 1024);
   w.kr = take(es * T * P->shape.Hkv * kD * P->max_ver, 1024);
   w.vp = take(es * T * P->shape.Hkv * kD, 1024);
   w.total = align_up(o, 1024);
@@ -370,6 +374,7 @@ PlanDev device_view(const akv_plan *P, void *ws) {
   d.n_mask = (int32_t)P->mwin.size();
   d.order = (const int32_t *)(b + w.order);
   d.qr = b + w.qr;
+  d.qcs = (float2 *)(b + w.qcs);
   d.kr = b + w.kr;
   d.vp = b + w.vp;
   d.T = P->T;
@@ -801,14 +806,16 @@ akv_status akv_segment_prepare(const akv_plan *P, const void *q, const void *k, 
   return AKV_OK;
 }
 
-akv_status akv_segment_attend(const akv_plan *P, void *out, void *workspace,
+akv_status akv_segment_attend(const akv_plan *P, const void *q, void *out, void *workspace,
                               size_t workspace_bytes, akv_stream_t stream) {
   AKV_ENTRY("akv_segment_attend");
   if (!P) return fail(AKV_ERR_INVALID, "plan is NULL");
   if (P->T == 0) return AKV_OK;
   if (!out) return fail(AKV_ERR_INVALID, "NULL output");
+  if (P->shape.dtype == AKV_BF16 && !q) return fail(AKV_ERR_INVALID, "NULL queries");
   if (akv_status st = check_run(P, workspace, workspace_bytes)) return st;
   PlanDev d = device_view(P, workspace);
+  d.q = q;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = P->shape.dtype == AKV_F32 ? launch_attn_simt_f32(d, out, s)
                                             : launch_attn_tc_bf16(d, out, s);
@@ -826,7 +833,7 @@ akv_status akv_segment_attention_run(const akv_plan *P, const void *q, const voi
   if (akv_status st = check_run(P, workspace, workspace_bytes)) return st;
   if (akv_status st = akv_segment_prepare(P, q, k, v, workspace, workspace_bytes, stream))
     return st;
-  return akv_segment_attend(P, out, workspace, workspace_bytes, stream);
+  return akv_segment_attend(P, q, out, workspace, workspace_bytes, stream);
 }
 
 size_t akv_segment_attention_workspace(const akv_shape *shape, int32_t n_req,

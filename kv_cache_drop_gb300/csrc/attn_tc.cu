@@ -1,9 +1,10 @@
 // bf16 segment-batch attention on the 5th-generation tensor cores (tcgen05,
 // TMEM accumulators, TMA loads), sm_103a.
 //
-// Operands: rotated Q and K and the permuted V are fp16 copies (see the
-// pre-pass); P is produced as fp16 by a packed fp16 exp; both products
-// accumulate in fp32.  Row sums of P come from the tensor core too: the PV
+// Operands: rotated K and the permuted V are fp16 copies (see the
+// pre-pass); each softmax thread rotates its own query row (raw bf16 row,
+// cos/sin from the pre-pass's per-row table) to fp16 as it loads it; P is
+// produced as fp16 by a packed fp16 exp; both products accumulate in fp32.  Row sums of P come from the tensor core too: the PV
 // product runs with N = 80, its B operand being the V tile (columns 0-63)
 // followed by a constant tile of ones (columns 64-79), so column 64 of the
 // accumulator is the row sum and the softmax threads never add.
@@ -103,6 +104,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = 2 * pair, g = h0 / grp;
   const int n_win = qt.win_cnt;
   const int T = (int)p.T;
+
+  // softmax threads: this row's raw query and cos/sin, loaded first so that
+  // their memory latency overlaps the CTA's set-up below
+  uint4 qraw[8];
+  float4 qcs[16];
+  if (warp < kProdWarp) {
+    const int row = threadIdx.x & 127, t = qt.t0 + row;
+    if (row < qt.len) {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          static_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)t * p.Hq + h0 + (warp >> 2)) * kD);
+      const float4 *cs4 = reinterpret_cast<const float4 *>(p.qcs + (int64_t)t * (kD / 2));
+#pragma unroll
+      for (int c = 0; c < 8; ++c) qraw[c] = __ldg(qrow + c);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) qcs[c] = __ldg(cs4 + c);
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) ptx::mbar_init(&sm.bar_kv[s], 1);
@@ -222,18 +240,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + i * 128;
     const uint32_t tO = tmem + lane_base + 256 + i * 80;
     const uint32_t tL = tO + 64;  // row sums
-    {  // this row's rotated query (fp16, 64 dims = 32 packed words) into TMEM
-      const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const __half *>(p.qr) +
-                                                          ((int64_t)(h0 + i) * T + t) * kD);
+    {  // this row's query rotated at its position, as fp16 (64 dims = 32
+       // packed words) into TMEM: the raw bf16 row and the row's cos/sin
+       // from the pre-pass's table (loaded at the start); the pair
+       // (d, d + 32) turns by angle d, in fp32 as the pre-pass rotates keys
       uint32_t qw[32];
+      bool ovf = false;
+      if (valid) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 x = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-        qw[4 * c] = x.x;
-        qw[4 * c + 1] = x.y;
-        qw[4 * c + 2] = x.z;
-        qw[4 * c + 3] = x.w;
+        for (int c = 0; c < 4; ++c) {  // dims 8c..8c+7 with 8c+32..8c+39
+          float x1[8], x2[8], y1[8], y2[8];
+          chunk_to_f32<__nv_bfloat16>(qraw[c], x1);
+          chunk_to_f32<__nv_bfloat16>(qraw[c + 4], x2);
+          float big = 0.f;
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float4 t4 = qcs[4 * c + e2];  // (cos, sin) of dims 8c+2e2, +1
+            const float co[2] = {t4.x, t4.z}, si[2] = {t4.y, t4.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e2 + h;
+              y1[e] = x1[e] * co[h] - x2[e] * si[h];
+              y2[e] = x1[e] * si[h] + x2[e] * co[h];
+              big = fmaxf(big, fmaxf(fabsf(y1[e]), fabsf(y2[e])));
+            }
+          }
+          ovf |= !(big <= 65504.f);
+          const uint4 a = f32_to_chunk<__half>(y1), b = f32_to_chunk<__half>(y2);
+          qw[4 * c] = a.x;
+          qw[4 * c + 1] = a.y;
+          qw[4 * c + 2] = a.z;
+          qw[4 * c + 3] = a.w;
+          qw[16 + 4 * c] = b.x;
+          qw[16 + 4 * c + 1] = b.y;
+          qw[16 + 4 * c + 2] = b.z;
+          qw[16 + 4 * c + 3] = b.w;
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 32; ++w) qw[w] = 0u;
       }
+      if (ovf) atomicOr(p.status, kStatusFp16Range);
       ptx::tmem_st32(tmem + lane_base + 416 + 32 * i, qw);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();

@@ -1,7 +1,11 @@
 // Restoration pre-pass (paper review page, Appendix A.1.1: "per-segment
 // temporary KV versions made by key rotation and value copy").
 //
-//  * Qr[h][t]     = R(pos(t)) Q[t][h]            rows in logical order
+//  * Qr[h][t]     = R(pos(t)) Q[t][h]            fp32 inputs: rows in logical
+//                                                  order; bf16 inputs: only
+//                                                  the cos/sin of each row's
+//                                                  angles, the attention
+//                                                  kernel rotates Q itself
 //  * Kr[v][g][j]  = R(pos_v(src(j))) K[src(j)][g] one copy per key version,
 //                                                  slots in the plan's order
 //  * Vp[g][j]     = V[src(j)][g]                  values copied once, shared
@@ -49,6 +53,24 @@ __global__ void __launch_bounds__(kThreads) prep_q_kernel(PlanDev p, const T *__
     ovf |= rotate_pair<T, TR>(src, dst, c, cs[r], sn[r]);
   }
   if (sizeof(TR) == 2 && ovf) atomicOr(p.status, kStatusFp16Range);
+}
+
+// bf16: cos/sin(pos(t) theta_f) for every row and frequency (the same
+// values prep_q_kernel uses); the attention kernel rotates each query row
+// with them as it loads it.
+__global__ void __launch_bounds__(kThreads) prep_qcs_kernel(PlanDev p, RopeTheta th) {
+  __shared__ ThetaSmem ts;
+  stage_theta(th, ts);
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kRows;
+  for (int i = threadIdx.x; i < kRows * (kD / 2); i += kThreads) {
+    const int r = i / (kD / 2), f = i % (kD / 2);
+    if (t0 + r < p.T) {
+      float c, s;
+      rope_cs(th, ts, f, p.tok_qpos[t0 + r], &c, &s);
+      p.qcs[(t0 + r) * (kD / 2) + f] = make_float2(c, s);
+    }
+  }
 }
 
 template <typename T, typename TR>
@@ -116,7 +138,10 @@ template <typename T, typename TR>
 cudaError_t prep(const PlanDev &p, const void *q, const void *k, const void *v,
                  const RopeTheta &th, cudaStream_t s) {
   const unsigned nb = (unsigned)((p.T + kRows - 1) / kRows);
-  prep_q_kernel<T, TR><<<nb, kThreads, 0, s>>>(p, (const T *)q, th);
+  if constexpr (std::is_same<T, float>::value)
+    prep_q_kernel<T, TR><<<nb, kThreads, 0, s>>>(p, (const T *)q, th);
+  else
+    prep_qcs_kernel<<<nb, kThreads, 0, s>>>(p, th);
   dim3 g2(nb, p.max_ver + 1);
   prep_kv_kernel<T, TR><<<g2, kThreads, 0, s>>>(p, (const T *)k, (const T *)v, th);
   return cudaGetLastError();
