@@ -213,3 +213,27 @@ def test_calls_do_not_wait_for_the_stream():
     ou, op = oracle.compact(*r.ops(), upto=-1)
     np.testing.assert_array_equal(idx[:n].cpu().numpy(), ou)
     np.testing.assert_array_equal(pos[:n].cpu().numpy(), op)
+
+
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_prefill_reports_fp16_range(which):
+    """A query (rotated in the attention kernel's load path) or a key (rotated
+    by the pre-pass) beyond the fp16 range of the tensor-core operands sets
+    status bit 2; the same request without it reports 0."""
+    import copy
+    torch = _torch_mod()
+    r = workloads.random_request(90, n_msgs=3, max_len=100, Hq=8, Hkv=2, dtype="bf16",
+                                 min_len=20)
+    shp = akv.shape(8, 2, 64, "bf16")
+    for big in (False, True):
+        rr = copy.deepcopy(r)
+        if big:
+            arr = getattr(rr, which)
+            arr[r.T // 2, 1, 3] = workloads.bf16_bits(np.array([1.0e5], np.float32))[0]
+        plan = akv.Plan(shp, [0, rr.T], [rr.ops()])
+        q, k, v = (akv.to_device(x, "bf16") for x in (rr.q, rr.k, rr.v))
+        out = torch.zeros_like(q)
+        ws = plan.workspace()
+        akv.akv_segment_attention_run(plan, q, k, v, out, ws)
+        torch.cuda.synchronize()
+        assert akv.akv_workspace_status(ws) == (2 if big else 0), (which, big)
