@@ -511,9 +511,10 @@ def decode_part(dw, warmup_steps=8):
                                     note="akv_append_kv + akv_decode_attention"),
                 rotate_on_read=dict(ms_per_step=ms_rope / dw.steps,
                                     bytes_per_step=bytes_rope / dw.steps,
-                                    gbs=bytes_rope / ms_rope / 1e6, launches_per_step=1,
-                                    memsets_per_step=1,
-                                    note="raw-key pool, per-entry positions, append fused"))
+                                    gbs=bytes_rope / ms_rope / 1e6, launches_per_step=2,
+                                    memsets_per_step=0,
+                                    note="raw-key pool, per-entry positions, append fused; "
+                                         "chunk partials merged by a second launch"))
 
 
 def decoder_part(mw, steps=3):

@@ -7,7 +7,9 @@
 // sum l, unnormalised output o) for the Hq/Hkv query heads of group g; the
 // partials are merged by their log-sum-exp -- for bf16 inside the same
 // launch, by the last CTA of each (request, KV head) to finish; for fp32 by
-// a combine kernel.
+// a combine kernel.  bf16 with rotation on read and 4 or 8 KV heads takes
+// all KV heads of a chunk per CTA (the rotation angles are shared) and
+// merges in a second launch.
 //
 // bf16: the group's query heads form the rows of an m16n8k16 tensor-core tile
 // (S = Q K^T with K rows as the B operand, then O += P V with P reused from
@@ -28,7 +30,7 @@ constexpr int kChunk = 2048;     // keys per CTA of the fp32 kernel
 constexpr int kMinChunk = 1024;  // bf16: chunk chosen per call in [kMinChunk, kMaxChunk]
 constexpr int kMaxChunk = 4096;
 constexpr int kMaxSplits = 1000;  // bf16: the in-kernel merge's weights fit shared memory
-constexpr int kRChunk = 512;  // keys per CTA of the fp32 rotate-on-read kernel
+constexpr int kRChunk = 512;  // fp32 rotate-on-read: keys per CTA; bf16 all-heads: the least
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;
 constexpr int kStages = 2;
@@ -50,6 +52,14 @@ Partials partials(void *ws, int B, int Hq, int max_kv, int chunk = kChunk) {
   const size_t ml_bytes = ((size_t)B * Hq * ns * 2 * 4 + 255) / 256 * 256;
   p.o = (float *)((char *)ws + ml_bytes);
   return p;
+}
+
+int device_sms() {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  return sms;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -582,6 +592,397 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 decode with rotation on read, all KV heads of a key chunk in one CTA.
+// The rotation of a key needs cos/sin of (position x frequency), the same
+// for every KV head; here a CTA takes (key chunk, request) with one warp per
+// KV head (kHkv = 4 or 8 warps), and the CTA fills, one tile ahead, a shared
+// table of the 16 x 32 cos/sin pairs of each 16-key tile, which every head's
+// warp then reads.  A thread's share of the next table is computed into
+// registers in the middle of the current tile's arithmetic and stored after
+// it, so the sin/cos latency overlaps that work; one barrier per tile then
+// publishes the table and frees the previous one.  The per-head work is the
+// per-head kernel's: 16-key tiles gathered by cp.async (the warps together
+// read a key's whole K and V rows), keys rotated in fp32 and rounded to
+// fp16, the query split into fp16 hi + lo, S in fp16 MMAs, online softmax,
+// P.V in bf16.  Each CTA leaves its chunk's partial (m, l, o) per query
+// head; a second launch merges them (decode_merge_heads_kernel): merged in
+// this kernel by the last CTA of a request, the whole request's merge (all
+// its query heads over all its chunks) ran in one CTA at the end of the
+// launch and made the step 12 % slower.
+// ---------------------------------------------------------------------------
+constexpr int kHStages = 2;  // K/V tiles in flight per warp (incl. the one in use)
+// table row of one key: 32 (cos, sin) pairs padded to 40 so that the two
+// keys read by one 8-lane phase of a 16-byte load fall in different banks
+constexpr int kTabRow = kD / 2 + 8;
+constexpr int kTabBytes = kTileKeys * kTabRow * 8;  // one tile's cos/sin table
+constexpr int kHeadsWaves = 8;  // CTA waves (2 per SM) aimed for when choosing the chunk
+
+// cos/sin of pos * theta_f beyond 2^18 (the double path); rare, so out of line
+__device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
+  float2 r;
+  rope_cs(theta, (double)pos, &r.x, &r.y);
+  return r;
+}
+
+template <int kHkv>
+__global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
+    decode_rope_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
+                             const int32_t *__restrict__ qpos, __nv_bfloat16 *kp,
+                             __nv_bfloat16 *vp, const int32_t *__restrict__ indptr,
+                             const int32_t *__restrict__ indices, Partials part, RopeTheta th,
+                             __nv_bfloat16 *out, const __nv_bfloat16 *k_new,
+                             const __nv_bfloat16 *v_new, const int32_t *new_slot, int chunk,
+                             const int32_t *__restrict__ kvpos) {
+  constexpr int kThreads = kHkv * 32;
+  constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
+  constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (2 or 4)
+  constexpr int kSB = 4096;                   // one stage: K tile 2 KiB | V tile 2 KiB
+  // dynamic smem: [warp][kHStages][stage], then two cos/sin tables
+  // [16 keys][kTabRow] float2
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float cs[kD / 2], sn[kD / 2];
+  __shared__ ThetaSmem ts;
+  __shared__ double thd[kD / 2];
+  const int split = blockIdx.x, b = blockIdx.y;
+  const int ns = gridDim.x;
+  const int grp = Hq / kHkv;
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;  // warp = KV head
+  const int gid = lane >> 2, tig = lane & 3;
+  const int beg = indptr[b], n = indptr[b + 1] - beg;
+  const int c0 = split * chunk, c1 = min(n, c0 + chunk);
+  if (c0 >= n) {  // the merge reads only the splits that hold keys
+    if (n <= 0 && split == 0)  // a request with no keys gets zeros
+      for (int i = threadIdx.x; i < Hq * kD; i += kThreads)
+        out[(int64_t)b * Hq * kD + i] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  float2 *tabs = reinterpret_cast<float2 *>(smem + kHkv * kHStages * kSB);
+  const int nk = c1 - c0;
+  const int n_tiles = (nk + kTileKeys - 1) / kTileKeys;
+  // this thread's table entries: key tkey of the tile, frequencies tf..tf+kFpt-1
+  const int tkey = threadIdx.x / kTpk, tf = (threadIdx.x % kTpk) * kFpt;
+  auto load_pos = [&](int t) {
+    const int k = t * kTileKeys + tkey;
+    return t < n_tiles && k < nk ? __ldg(kvpos + beg + c0 + k) : 0;
+  };
+  auto angles = [&](int pos, float4 *cs4) {
+    const bool wide = pos < -262144 || pos > 262144;
+#pragma unroll
+    for (int j = 0; j < kFpt / 2; ++j) {
+      const int f = tf + 2 * j;
+      if (wide) {
+        const float2 a = rope_cs_wide(thd[f], pos), c = rope_cs_wide(thd[f + 1], pos);
+        cs4[j] = make_float4(a.x, a.y, c.x, c.y);
+      } else {
+        rope_cs_fast(ts.hi[f], ts.lo[f], pos, &cs4[j].x, &cs4[j].y);
+        rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &cs4[j].z, &cs4[j].w);
+      }
+    }
+  };
+  auto store_tab = [&](int t, const float4 *cs4) {
+    float4 *row = reinterpret_cast<float4 *>(tabs + (t & 1) * (kTileKeys * kTabRow) +
+                                             tkey * kTabRow + tf);
+#pragma unroll
+    for (int j = 0; j < kFpt / 2; ++j) row[j] = cs4[j];
+  };
+  // positions of the next tiles' table keys, loaded three tiles ahead
+  int pos1 = load_pos(1), pos2 = load_pos(2), pos3 = load_pos(3);
+  const int pos0 = load_pos(0);
+
+  if (threadIdx.x < kD / 2) {
+    rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
+    thd[threadIdx.x] = th.th[threadIdx.x];
+  }
+  stage_theta(th, ts);
+  if (new_slot && c1 == n) {  // fused append of the step's token (raw key: a copy)
+    const int64_t src = ((int64_t)b * kHkv + g) * kD, dst = ((int64_t)new_slot[b] * kHkv + g) * kD;
+    if (lane < kD / 8)
+      reinterpret_cast<uint4 *>(kp + dst)[lane] = reinterpret_cast<const uint4 *>(k_new + src)[lane];
+    else if (lane < kD / 4)
+      reinterpret_cast<uint4 *>(vp + dst)[lane - kD / 8] =
+          reinterpret_cast<const uint4 *>(v_new + src)[lane - kD / 8];
+  }
+  __syncthreads();  // frequencies staged, the appended row visible
+  {
+    float4 c4[kFpt / 2];
+    angles(pos0, c4);
+    store_tab(0, c4);
+  }
+
+  uint8_t *wsm = smem + g * kHStages * kSB;
+  const uint32_t wsm_u = smem_u32(wsm);
+  // pool slot of key `lane` of tile t (0 past the end), loaded one tile
+  // ahead of its use
+  auto load_slot = [&](int t) {
+    const int k = t * kTileKeys + lane;
+    return lane < kTileKeys && k < nk ? __ldg(indices + beg + c0 + k) : 0;
+  };
+  auto issue = [&](int t, int slot) {
+    const int stage = t % kHStages;
+    if (t < n_tiles) {
+      const int k0 = t * kTileKeys;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = lane + 32 * i;  // 128 chunks per tile: key = idx/8, chunk = idx%8
+        const int key = idx >> 3, ch = idx & 7;
+        const int sl = __shfl_sync(0xffffffffu, slot, key);
+        const bool valid = k0 + key < nk;
+        const int64_t off = ((int64_t)sl * kHkv + g) * kD + ch * 8;
+        cp_async16(wsm_u + stage * kSB + swz(key, ch), kp + off, valid);
+        cp_async16(wsm_u + stage * kSB + 2048 + swz(key, ch), vp + off, valid);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
+  };
+  int slot_nx = load_slot(0);
+#pragma unroll
+  for (int t = 0; t < kHStages - 1; ++t) {
+    const int sl = slot_nx;
+    slot_nx = load_slot(t + 1);
+    issue(t, sl);
+  }
+
+  // Q fragments of this warp's head group (rows = its query heads, 16 rows
+  // padded with zeros), rotated at the query position, 1/sqrt(D) * log2(e)
+  // folded in, split into fp16 hi + lo
+  uint32_t qa[4][4], ql[4][4];
+  {
+    const float qsc = 0.125f * kLog2e;
+    float qv[2][16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = gid + 8 * hh;
+      const bool ok = row < grp;
+      const __nv_bfloat16 *qrow = q + ((int64_t)b * Hq + g * grp + (ok ? row : 0)) * kD;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          qv[hh][ks * 4 + e] = ok ? __bfloat162float(qrow[d]) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = ks * 16 + 2 * tig + (e & 1) + (e >> 1) * 8;
+          const float x1 = qv[hh][ks * 4 + e], x2 = qv[hh][(ks + 2) * 4 + e];
+          qv[hh][ks * 4 + e] = (x1 * cs[d] - x2 * sn[d]) * qsc;
+          qv[hh][(ks + 2) * 4 + e] = (x1 * sn[d] + x2 * cs[d]) * qsc;
+        }
+    auto lo = [](float x) { return x - __half2float(__float2half_rn(x)); };
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
+      qa[ks][0] = pack_f16(a0[0], a0[1]);
+      qa[ks][1] = pack_f16(a1[0], a1[1]);
+      qa[ks][2] = pack_f16(a0[2], a0[3]);
+      qa[ks][3] = pack_f16(a1[2], a1[3]);
+      ql[ks][0] = pack_f16(lo(a0[0]), lo(a0[1]));
+      ql[ks][1] = pack_f16(lo(a1[0]), lo(a1[1]));
+      ql[ks][2] = pack_f16(lo(a0[2]), lo(a0[3]));
+      ql[ks][3] = pack_f16(lo(a1[2]), lo(a1[3]));
+    }
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  __syncthreads();  // table 0 complete
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int sl = slot_nx;
+    slot_nx = load_slot(it + kHStages);
+    issue(it + kHStages - 1, sl);
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kHStages - 1));
+    __syncwarp();
+    const float2 *tab = tabs + (it & 1) * (kTileKeys * kTabRow);
+    const uint32_t kt = wsm_u + (it % kHStages) * kSB, vt = kt + 2048;
+    const int k0 = it * kTileKeys;
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      uint32_t kb[4][4];
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int mi = lane >> 3;
+        const int key = (mi >> 1) * 8 + (lane & 7);
+        const int ch = ks * 2 + (mi & 1);
+        ldsm_x4(kt + swz(key, ch), kb[ks][0], kb[ks][1], kb[ks][2], kb[ks][3]);
+      }
+      // rotate: the pair (d, d + 32) of keys gid and gid + 8 sits in k-steps
+      // ks and ks + 2 of this lane; frequencies f = 16ks + 8h + 2tig, f + 1
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
+          const int key = gid + 8 * (r >> 1);
+          const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
+          const float4 t = *reinterpret_cast<const float4 *>(tab + key * kTabRow + f);
+          __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
+          __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
+          const float x1a = __low2float(a), x1b = __high2float(a);
+          const float x2a = __low2float(bq), x2b = __high2float(bq);
+          const float y1a = x1a * t.x - x2a * t.y, y1b = x1b * t.z - x2b * t.w;
+          const float y2a = x1a * t.y + x2a * t.x, y2b = x1b * t.w + x2b * t.z;
+          kb[ks][r] = pack_f16(y1a, y1b);
+          kb[ks + 2][r] = pack_f16(y2a, y2b);
+        }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_f16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+        mma_f16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+        mma_f16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+        mma_f16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+      }
+    }
+    // the next tile's angles (stored after this tile's arithmetic)
+    float4 nxt[kFpt / 2];
+    angles(pos1, nxt);
+    pos1 = pos2;
+    pos2 = pos3;
+    pos3 = load_pos(it + 4);
+    // mask the ragged tail; online softmax in log2 units
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = k0 + nb * 8 + 2 * tig + (e & 1);
+        if (key >= nk) s[nb][e] = -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+      }
+    float alpha[2], mref[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mn = fmaxf(m[r], mx[r]);
+      mref[r] = mn == -INFINITY ? 0.f : mn;
+      alpha[r] = exp2f(m[r] - mref[r]);
+      m[r] = mn;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nb][e] = exp2f(s[nb][e] - mref[e >> 1]);
+        rs[e >> 1] += s[nb][e];
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + rs[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    // O += P V: P from the S accumulators (keys as k), V through ldmatrix.trans
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int nb2 = 0; nb2 < 4; ++nb2) {
+      const int mi = lane >> 3;
+      const int key = (mi & 1) * 8 + (lane & 7);
+      const int ch = nb2 * 2 + (mi >> 1);
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vt + swz(key, ch), v0, v1, v2, v3);
+      mma_bf16(o[2 * nb2], pa, v0, v1);
+      mma_bf16(o[2 * nb2 + 1], pa, v2, v3);
+    }
+    // publish the next table; every warp is done with this one (its buffer
+    // is the one the following iteration fills)
+    if (it + 1 < n_tiles) store_tab(it + 1, nxt);
+    __syncthreads();
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::);
+
+  // this warp's split partial: rows gid and gid + 8 (query heads of its
+  // group), columns 8i + 2tig (+1)
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int row = gid + 8 * hh;
+    if (row < grp) {
+      const int64_t pi = ((int64_t)b * Hq + g * grp + row) * ns + split;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<float2 *>(part.o + pi * kD + i * 8 + 2 * tig) =
+            make_float2(o[i][2 * hh], o[i][2 * hh + 1]);
+      if (tig == 0) {
+        part.ml[2 * pi] = m[hh];
+        part.ml[2 * pi + 1] = l[hh];
+      }
+    }
+  }
+}
+
+// Merge of the chunk partials of decode_rope_heads_kernel: a CTA per (query
+// head, request); the chunk weights 2^(m_s - M) and 1 / L from one warp,
+// then 16 groups of 16 threads each sum every 16th chunk's output row
+// (4 columns per thread) and the groups' sums are added in shared memory.
+// A request with no keys gets zeros.
+__global__ void __launch_bounds__(256) decode_merge_heads_kernel(int Hq, int ns, int chunk,
+                                                                 const int32_t *indptr,
+                                                                 Partials part,
+                                                                 __nv_bfloat16 *out) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int n = indptr[b + 1] - indptr[b];
+  const int used = n <= 0 ? 0 : min(ns, (n + chunk - 1) / chunk);
+  const int64_t base = ((int64_t)b * Hq + h) * ns;
+  __shared__ float wsm[kMaxSplits];
+  __shared__ float4 red[16][kD / 4];
+  __shared__ float rl;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = lane; s < used; s += 32) M = fmaxf(M, __ldcg(part.ml + 2 * (base + s)));
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Mr = M == -INFINITY ? 0.f : M;
+    float L = 0.f;
+    for (int s = lane; s < used; s += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part.ml) + base + s);
+      const float f = exp2f(ml.x - Mr);
+      wsm[s] = f;
+      L += ml.y * f;
+    }
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) rl = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  const int cg = threadIdx.x & 15, sg = threadIdx.x >> 4;  // 4-column group, chunk group
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = sg; s < used; s += 16) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(part.o + (base + s) * kD) + cg);
+    const float w = wsm[s];
+    acc.x += v.x * w;
+    acc.y += v.y * w;
+    acc.z += v.z * w;
+    acc.w += v.w * w;
+  }
+  red[sg][cg] = acc;
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    const int col = threadIdx.x;
+    float x = 0.f;
+    for (int j = 0; j < 16; ++j) x += reinterpret_cast<const float *>(&red[j][col >> 2])[col & 3];
+    out[((int64_t)b * Hq + h) * kD + col] = __float2bfloat16_rn(x * rl);
+  }
+}
+
 // fp32: thread per key, block of 128 threads per (split, query head, request)
 __global__ void __launch_bounds__(128)
     decode_f32_kernel(int Hq, int Hkv, const float *__restrict__ q, const int32_t *__restrict__ qpos,
@@ -799,8 +1200,10 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_kv) {
 }
 
 size_t decode_rope_workspace_bytes(int dtype, int B, int Hq, int Hkv, int max_kv) {
-  return dtype == AKV_BF16 ? decode_workspace_bytes(B, Hq, Hkv, max_kv)
-                           : decode_partials_bytes(B, Hq, max_kv, true);
+  // partials for the most splits (chunks of kRChunk keys); bf16 adds the
+  // merge counters of the per-head kernel
+  if (dtype != AKV_BF16) return decode_partials_bytes(B, Hq, max_kv, true);
+  return decode_partials_bytes(B, Hq, max_kv, true) + ((size_t)B * Hkv * 4 + 255) / 256 * 256;
 }
 
 namespace {
@@ -812,17 +1215,39 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         const int32_t *kvpos = nullptr) {
   // chunk: the largest of 4096, 2048, 1024 keys that still gives about two
   // waves of CTAs (4 per SM) when every request is max_kv long
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
+  const int sms = device_sms();
   int chunk = kMaxChunk;
   while (chunk > kMinChunk && (int64_t)B * n_splits(max_kv, chunk) * Hkv < 2LL * 4 * sms) chunk /= 2;
   while (n_splits(max_kv, chunk) > kMaxSplits) chunk *= 2;
   const int ns = n_splits(max_kv, chunk);
   Partials part = partials(ws, B, Hq, max_kv, chunk);
-  int *counters = reinterpret_cast<int *>(static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv));
   const bool rope = kvpos != nullptr;
+  int *counters = reinterpret_cast<int *>(
+      static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv, rope));
+  if (rope && (Hkv == 4 || Hkv == 8)) {
+    // all KV heads of a chunk in one CTA of Hkv warps (two CTAs per SM for
+    // 8 heads, three for 4: shared memory); the chunk is the largest that
+    // still gives about kHeadsWaves waves of CTAs when every request is
+    // max_kv long; then the merge launch
+    const int per_sm = Hkv == 8 ? 2 : 3;
+    int rc = kMaxChunk;
+    while (rc > kRChunk && (int64_t)B * n_splits(max_kv, rc) < (int64_t)kHeadsWaves * per_sm * sms)
+      rc /= 2;
+    while (n_splits(max_kv, rc) > kMaxSplits) rc *= 2;
+    const int rns = n_splits(max_kv, rc);
+    Partials rpart = partials(ws, B, Hq, max_kv, rc);
+    const int rsmem = Hkv * kHStages * 4096 + 2 * kTabBytes;
+    auto kern = Hkv == 8 ? decode_rope_heads_kernel<8> : decode_rope_heads_kernel<4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(rns, B), Hkv * 32, rsmem, s>>>(
+        Hq, (const __nv_bfloat16 *)q, qpos, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
+        indices, rpart, th, (__nv_bfloat16 *)out, (const __nv_bfloat16 *)k_new,
+        (const __nv_bfloat16 *)v_new, new_slot, rc, kvpos);
+    decode_merge_heads_kernel<<<dim3(Hq, B), 256, 0, s>>>(Hq, rns, rc, indptr, rpart,
+                                                          (__nv_bfloat16 *)out);
+    return cudaGetLastError();
+  }
   // dynamic shared memory: the tile buffers, or the merge's per-split
   // weights ([16 rows][ns] floats and 16 row totals) when those are larger
   const int smem = std::max(kWarps * kStages * kStageBytes(rope), (16 * ns + 16) * 4);

@@ -471,6 +471,81 @@ def test_decode_rope_repos_by_positions():
         assert_close(res[step], ref, "bf16")
 
 
+def test_decode_rope_many_splits():
+    """One request of a million raw keys behind a single KV head with 16
+    query heads: about a thousand key chunks, so the merge of the splits
+    runs in several passes of a few query heads each; the positions pass
+    2^18 (the double-precision angle path)."""
+    dw = workloads.decode_workload(seed=31, B=1, active=(1_000_000, 1_000_000), steps=1, Hq=16,
+                                   Hkv=1)
+    pos = _rope_positions(dw, seed=32)
+    res, _, _ = _run_decode_rope(dw, {0}, pos)
+    assert_close(res[0], _decode_rope_oracle(dw, 0, pos, oracle.widen(dw.q[0], "bf16")), "bf16")
+
+
+def test_decode_rope_more_than_eight_kv_heads():
+    """16 KV heads (two query heads each): more KV heads than one CTA of the
+    all-heads kernel takes, so the per-head kernel runs."""
+    dw = workloads.decode_workload(seed=33, B=3, active=(200, 4000), steps=2, Hq=32, Hkv=16)
+    pos = _rope_positions(dw, seed=34)
+    res, _, _ = _run_decode_rope(dw, {0, 1}, pos)
+    for step, got in res.items():
+        assert_close(got, _decode_rope_oracle(dw, step, pos, oracle.widen(dw.q[step], "bf16")),
+                     "bf16")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 8), (16, 4)])
+def test_decode_rope_even_split_edges(Hq, Hkv):
+    """Rotation on read with 4 or 8 KV heads (the kernel that splits the
+    step's entries evenly over one wave of CTAs): requests with no entry, one
+    entry, 15/16/17 entries (tile edges), many short requests sharing a CTA's
+    range, two long ones spanning many CTAs, positions past 2^18 and a
+    negative one; no fused append."""
+    torch = _torch()
+    rng = np.random.default_rng(41)
+    lens = [0, 1, 15, 16, 17, 0, 5000, 3, 2, 1, 0, 33, 64, 9000, 0, 7] + \
+        [int(x) for x in rng.integers(0, 40, size=60)]
+    B, S = len(lens), 20000
+    shp = akv.shape(Hq, Hkv, 64, "bf16")
+    kpool = workloads.bf16_bits(rng.standard_normal((S, Hkv, 64)).astype(np.float32))
+    vpool = workloads.bf16_bits(rng.standard_normal((S, Hkv, 64)).astype(np.float32))
+    q = workloads.bf16_bits(rng.standard_normal((B, Hq, 64)).astype(np.float32))
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    idx = rng.integers(0, S, size=int(indptr[-1])).astype(np.int32)
+    pos, qpos = [], []
+    for b, n in enumerate(lens):
+        base = [0, 300_000, 3_000_000][b % 3]
+        p = base + np.sort(rng.choice(4 * n + 8, size=n, replace=False))
+        if b == 6:
+            p[0] = -5
+        pos.append(p.astype(np.int32))
+        qpos.append(int(p[-1]) + 1 if n else base)
+    kvpos = np.concatenate(pos).astype(np.int32)
+    max_kv = max(lens)
+    out = torch.full((B, Hq, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(akv.akv_decode_rope_workspace(shp, B, max_kv), dtype=torch.uint8,
+                     device="cuda")
+    kp, vp = akv.to_device(kpool, "bf16"), akv.to_device(vpool, "bf16")
+    for _ in range(2):  # the merge counters are left at zero for the next call
+        akv.akv_decode_attention_rope(shp, B, akv.to_device(q, "bf16"), akv.i32_device(qpos),
+                                      None, None, None, kp, vp, akv.i32_device(indptr),
+                                      akv.i32_device(idx), akv.i32_device(kvpos), max_kv, out, ws)
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        ref = np.zeros((B, Hq, 64))
+        for b, n in enumerate(lens):
+            if n == 0:
+                continue
+            sl = idx[indptr[b]:indptr[b + 1]]
+            kr = oracle.rope(oracle.widen(kpool[sl], "bf16"), pos[b][:, None], 10000.0)
+            ref[b] = oracle.decode_attention(oracle.widen(q[b:b + 1], "bf16"),
+                                             np.array([qpos[b]]), kr,
+                                             oracle.widen(vpool[sl], "bf16"),
+                                             np.array([0, n]), np.arange(n), "f64", 10000.0)[0]
+        assert_close(got, ref, "bf16")
+        assert not np.any(got[np.array(lens) == 0])  # no entries: zeros
+
+
 def test_decode_rope_full_size():
     """14 requests, 20k-90k keys, GQA 64/8 (one CTA reads whole pool rows):
     256 steps with the append fused; steps 0 and 255 checked in full."""
