@@ -649,6 +649,8 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
   const int grp = Hq / kHkv;
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;  // warp = KV head
   const int gid = lane >> 2, tig = lane & 3;
+  // the merge launch may be placed once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int beg = indptr[b], n = indptr[b + 1] - beg;
   const int c0 = split * chunk, c1 = min(n, c0 + chunk);
   if (c0 >= n) {  // the merge reads only the splits that hold keys
@@ -931,10 +933,14 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
 }
 
 // Merge of the chunk partials of decode_rope_heads_kernel: a CTA per (query
-// head, request); the chunk weights 2^(m_s - M) and 1 / L from one warp,
-// then 16 groups of 16 threads each sum every 16th chunk's output row
-// (4 columns per thread) and the groups' sums are added in shared memory.
-// A request with no keys gets zeros.
+// head, request).  One warp folds the chunks' (m, l) pairs into (M, L) with
+// a running maximum (each chunk's m kept in shared memory), then every
+// thread turns the m into weights 2^(m_s - M), and 16 groups of 16 threads
+// each sum every 16th chunk's output row (4 columns per thread); the
+// groups' sums are added in shared memory.  A request with no keys gets
+// zeros.  Launched as a programmatic dependent of the attention kernel: its
+// CTAs are placed while the last attention CTAs run and wait (griddepcontrol
+// .wait) until that grid has finished and its partials are visible.
 __global__ void __launch_bounds__(256) decode_merge_heads_kernel(int Hq, int ns, int chunk,
                                                                  const int32_t *indptr,
                                                                  Partials part,
@@ -945,23 +951,34 @@ __global__ void __launch_bounds__(256) decode_merge_heads_kernel(int Hq, int ns,
   const int64_t base = ((int64_t)b * Hq + h) * ns;
   __shared__ float wsm[kMaxSplits];
   __shared__ float4 red[16][kD / 4];
-  __shared__ float rl;
+  __shared__ float mrow, rl;
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = lane; s < used; s += 32) M = fmaxf(M, __ldcg(part.ml + 2 * (base + s)));
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float Mr = M == -INFINITY ? 0.f : M;
-    float L = 0.f;
+    float M = -INFINITY, L = 0.f;
     for (int s = lane; s < used; s += 32) {
       const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part.ml) + base + s);
-      const float f = exp2f(ml.x - Mr);
-      wsm[s] = f;
-      L += ml.y * f;
+      wsm[s] = ml.x;
+      if (ml.x > M) {
+        L = L * exp2f(M - ml.x) + ml.y;
+        M = ml.x;
+      } else if (ml.x > -INFINITY) {
+        L += ml.y * exp2f(ml.x - M);
+      }
     }
-    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) rl = L > 0.f ? 1.f / L : 0.f;
+    for (int o = 16; o; o >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o), L2 = __shfl_xor_sync(0xffffffffu, L, o);
+      const float Mn = fmaxf(M, M2);
+      L = (M == -INFINITY ? 0.f : L * exp2f(M - Mn)) + (M2 == -INFINITY ? 0.f : L2 * exp2f(M2 - Mn));
+      M = Mn;
+    }
+    if (lane == 0) {
+      mrow = M == -INFINITY ? 0.f : M;
+      rl = L > 0.f ? 1.f / L : 0.f;
+    }
   }
+  __syncthreads();
+  for (int s = threadIdx.x; s < used; s += blockDim.x) wsm[s] = exp2f(wsm[s] - mrow);
   __syncthreads();
   const int cg = threadIdx.x & 15, sg = threadIdx.x >> 4;  // 4-column group, chunk group
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1244,9 +1261,20 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
         Hq, (const __nv_bfloat16 *)q, qpos, (__nv_bfloat16 *)kp, (__nv_bfloat16 *)vp, indptr,
         indices, rpart, th, (__nv_bfloat16 *)out, (const __nv_bfloat16 *)k_new,
         (const __nv_bfloat16 *)v_new, new_slot, rc, kvpos);
-    decode_merge_heads_kernel<<<dim3(Hq, B), 256, 0, s>>>(Hq, rns, rc, indptr, rpart,
-                                                          (__nv_bfloat16 *)out);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the merge as a programmatic dependent launch (it waits for this grid)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(Hq, B);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_heads_kernel, Hq, rns, rc, indptr, rpart,
+                              (__nv_bfloat16 *)out);
   }
   // dynamic shared memory: the tile buffers, or the merge's per-split
   // weights ([16 rows][ns] floats and 16 row totals) when those are larger
