@@ -625,9 +625,9 @@ __device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
   return r;
 }
 
-template <int kHkv>
+template <int kHkv, bool kRope>
 __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
-    decode_rope_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
+    decode_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
                              const int32_t *__restrict__ qpos, __nv_bfloat16 *kp,
                              __nv_bfloat16 *vp, const int32_t *__restrict__ indptr,
                              const int32_t *__restrict__ indices, Partials part, RopeTheta th,
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
   constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
   constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (2 or 4)
   constexpr int kSB = 4096;                   // one stage: K tile 2 KiB | V tile 2 KiB
-  // dynamic smem: [warp][kHStages][stage], then two cos/sin tables
+  // dynamic smem: [warp][kHStages][stage], then (kRope) two cos/sin tables
   // [16 keys][kTabRow] float2
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float cs[kD / 2], sn[kD / 2];
@@ -689,24 +689,39 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
     for (int j = 0; j < kFpt / 2; ++j) row[j] = cs4[j];
   };
   // positions of the next tiles' table keys, loaded three tiles ahead
-  int pos1 = load_pos(1), pos2 = load_pos(2), pos3 = load_pos(3);
-  const int pos0 = load_pos(0);
+  int pos1 = 0, pos2 = 0, pos3 = 0, pos0 = 0;
+  if (kRope) {
+    pos1 = load_pos(1);
+    pos2 = load_pos(2);
+    pos3 = load_pos(3);
+    pos0 = load_pos(0);
+  }
 
   if (threadIdx.x < kD / 2) {
     rope_cs_lane(th, threadIdx.x, qpos[b], &cs[threadIdx.x], &sn[threadIdx.x]);
-    thd[threadIdx.x] = th.th[threadIdx.x];
+    if (kRope) thd[threadIdx.x] = th.th[threadIdx.x];
   }
-  stage_theta(th, ts);
-  if (new_slot && c1 == n) {  // fused append of the step's token (raw key: a copy)
+  if (kRope) stage_theta(th, ts);
+  if (new_slot && c1 == n) {  // fused append of the step's token
     const int64_t src = ((int64_t)b * kHkv + g) * kD, dst = ((int64_t)new_slot[b] * kHkv + g) * kD;
-    if (lane < kD / 8)
-      reinterpret_cast<uint4 *>(kp + dst)[lane] = reinterpret_cast<const uint4 *>(k_new + src)[lane];
-    else if (lane < kD / 4)
-      reinterpret_cast<uint4 *>(vp + dst)[lane - kD / 8] =
-          reinterpret_cast<const uint4 *>(v_new + src)[lane - kD / 8];
+    if (kRope) {  // the pool keeps raw keys: a copy
+      if (lane < kD / 8)
+        reinterpret_cast<uint4 *>(kp + dst)[lane] = reinterpret_cast<const uint4 *>(k_new + src)[lane];
+      else if (lane < kD / 4)
+        reinterpret_cast<uint4 *>(vp + dst)[lane - kD / 8] =
+            reinterpret_cast<const uint4 *>(v_new + src)[lane - kD / 8];
+    } else {  // the key rotated at the query position (cos/sin above)
+      __syncthreads();
+      const int f = lane;
+      const float x1 = __bfloat162float(k_new[src + f]), x2 = __bfloat162float(k_new[src + f + kD / 2]);
+      kp[dst + f] = __float2bfloat16_rn(x1 * cs[f] - x2 * sn[f]);
+      kp[dst + f + kD / 2] = __float2bfloat16_rn(x1 * sn[f] + x2 * cs[f]);
+      if (lane < kD / 8)
+        reinterpret_cast<uint4 *>(vp + dst)[lane] = reinterpret_cast<const uint4 *>(v_new + src)[lane];
+    }
   }
   __syncthreads();  // frequencies staged, the appended row visible
-  {
+  if (kRope) {
     float4 c4[kFpt / 2];
     angles(pos0, c4);
     store_tab(0, c4);
@@ -747,7 +762,8 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
 
   // Q fragments of this warp's head group (rows = its query heads, 16 rows
   // padded with zeros), rotated at the query position, 1/sqrt(D) * log2(e)
-  // folded in, split into fp16 hi + lo
+  // folded in, split into hi + lo parts: fp16 with rotation on read (the
+  // score product takes fp16 keys), else bf16
   uint32_t qa[4][4], ql[4][4];
   {
     const float qsc = 0.125f * kLog2e;
@@ -776,18 +792,22 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
           qv[hh][ks * 4 + e] = (x1 * cs[d] - x2 * sn[d]) * qsc;
           qv[hh][(ks + 2) * 4 + e] = (x1 * sn[d] + x2 * cs[d]) * qsc;
         }
-    auto lo = [](float x) { return x - __half2float(__float2half_rn(x)); };
+    auto pk = [](float x, float y) { return kRope ? pack_f16(x, y) : pack_bf16(x, y); };
+    auto lo = [](float x) {
+      return kRope ? x - __half2float(__float2half_rn(x))
+                   : x - __bfloat162float(__float2bfloat16_rn(x));
+    };
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       const float *a0 = &qv[0][ks * 4], *a1 = &qv[1][ks * 4];
-      qa[ks][0] = pack_f16(a0[0], a0[1]);
-      qa[ks][1] = pack_f16(a1[0], a1[1]);
-      qa[ks][2] = pack_f16(a0[2], a0[3]);
-      qa[ks][3] = pack_f16(a1[2], a1[3]);
-      ql[ks][0] = pack_f16(lo(a0[0]), lo(a0[1]));
-      ql[ks][1] = pack_f16(lo(a1[0]), lo(a1[1]));
-      ql[ks][2] = pack_f16(lo(a0[2]), lo(a0[3]));
-      ql[ks][3] = pack_f16(lo(a1[2]), lo(a1[3]));
+      qa[ks][0] = pk(a0[0], a0[1]);
+      qa[ks][1] = pk(a1[0], a1[1]);
+      qa[ks][2] = pk(a0[2], a0[3]);
+      qa[ks][3] = pk(a1[2], a1[3]);
+      ql[ks][0] = pk(lo(a0[0]), lo(a0[1]));
+      ql[ks][1] = pk(lo(a1[0]), lo(a1[1]));
+      ql[ks][2] = pk(lo(a0[2]), lo(a0[3]));
+      ql[ks][3] = pk(lo(a1[2]), lo(a1[3]));
     }
   }
 
@@ -795,7 +815,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  __syncthreads();  // table 0 complete
+  if (kRope) __syncthreads();  // table 0 complete
 
   for (int it = 0; it < n_tiles; ++it) {
     const int sl = slot_nx;
@@ -819,7 +839,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
       // rotate: the pair (d, d + 32) of keys gid and gid + 8 sits in k-steps
       // ks and ks + 2 of this lane; frequencies f = 16ks + 8h + 2tig, f + 1
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks)
+      for (int ks = 0; ks < 2 && kRope; ++ks)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
           const int key = gid + 8 * (r >> 1);
@@ -836,18 +856,27 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
         }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_f16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
-        mma_f16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
-        mma_f16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
-        mma_f16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+        if (kRope) {
+          mma_f16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+          mma_f16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+          mma_f16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+          mma_f16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+        } else {
+          mma_bf16(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+          mma_bf16(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+          mma_bf16(s[0], ql[ks], kb[ks][0], kb[ks][1]);
+          mma_bf16(s[1], ql[ks], kb[ks][2], kb[ks][3]);
+        }
       }
     }
     // the next tile's angles (stored after this tile's arithmetic)
     float4 nxt[kFpt / 2];
-    angles(pos1, nxt);
-    pos1 = pos2;
-    pos2 = pos3;
-    pos3 = load_pos(it + 4);
+    if (kRope) {
+      angles(pos1, nxt);
+      pos1 = pos2;
+      pos2 = pos3;
+      pos3 = load_pos(it + 4);
+    }
     // mask the ragged tail; online softmax in log2 units
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -903,8 +932,12 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
     }
     // publish the next table; every warp is done with this one (its buffer
     // is the one the following iteration fills)
-    if (it + 1 < n_tiles) store_tab(it + 1, nxt);
-    __syncthreads();
+    if (kRope) {
+      if (it + 1 < n_tiles) store_tab(it + 1, nxt);
+      __syncthreads();
+    } else {
+      __syncwarp();
+    }
   }
   asm volatile("cp.async.wait_group 0;\n" ::);
 
@@ -932,7 +965,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
   }
 }
 
-// Merge of the chunk partials of decode_rope_heads_kernel: a CTA per (query
+// Merge of the chunk partials of decode_heads_kernel: a CTA per (query
 // head, request).  One warp folds the chunks' (m, l) pairs into (M, L) with
 // a running maximum (each chunk's m kept in shared memory), then every
 // thread turns the m into weights 2^(m_s - M), and 16 groups of 16 threads
@@ -1241,20 +1274,22 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
   const bool rope = kvpos != nullptr;
   int *counters = reinterpret_cast<int *>(
       static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv, rope));
-  if (rope && (Hkv == 4 || Hkv == 8)) {
+  if (Hkv == 4 || Hkv == 8) {
     // all KV heads of a chunk in one CTA of Hkv warps (two CTAs per SM for
     // 8 heads, three for 4: shared memory); the chunk is the largest that
     // still gives about kHeadsWaves waves of CTAs when every request is
     // max_kv long; then the merge launch
     const int per_sm = Hkv == 8 ? 2 : 3;
     int rc = kMaxChunk;
-    while (rc > kRChunk && (int64_t)B * n_splits(max_kv, rc) < (int64_t)kHeadsWaves * per_sm * sms)
+    const int floor = rope ? kRChunk : kMinChunk;  // the workspace holds that many splits
+    while (rc > floor && (int64_t)B * n_splits(max_kv, rc) < (int64_t)kHeadsWaves * per_sm * sms)
       rc /= 2;
     while (n_splits(max_kv, rc) > kMaxSplits) rc *= 2;
     const int rns = n_splits(max_kv, rc);
     Partials rpart = partials(ws, B, Hq, max_kv, rc);
-    const int rsmem = Hkv * kHStages * 4096 + 2 * kTabBytes;
-    auto kern = Hkv == 8 ? decode_rope_heads_kernel<8> : decode_rope_heads_kernel<4>;
+    const int rsmem = Hkv * kHStages * 4096 + (rope ? 2 * kTabBytes : 0);
+    auto kern = rope ? (Hkv == 8 ? decode_heads_kernel<8, true> : decode_heads_kernel<4, true>)
+                     : (Hkv == 8 ? decode_heads_kernel<8, false> : decode_heads_kernel<4, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);
     if (e != cudaSuccess) return e;
     kern<<<dim3(rns, B), Hkv * 32, rsmem, s>>>(
