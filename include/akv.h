@@ -354,7 +354,11 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
  * rotated).  q_pos, kv_indptr ([B+1]), kv_indices: device int32.  max_kv:
  * host, an upper bound on any request's length (sizes the split-KV grid).
  * out [B, Hq, D] device.  A request with no keys gets zeros.
- * Limits: B <= 65535; bf16: max_kv <= 2,048,000 (AKV_ERR_UNSUPPORTED). */
+ * Limits: B <= 65535; bf16: max_kv <= 2,048,000 (AKV_ERR_UNSUPPORTED).
+ * Work on `stream` (bf16): with 4 or 8 KV heads, the attention launch (one
+ * CTA per key chunk and request, all KV heads) and the split merge as a
+ * programmatic dependent launch; other head counts, a memset of B x Hkv
+ * merge counters and one launch that also merges. */
 size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
 akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
                                 const int32_t *q_pos, const void *k_pool, const void *v_pool,
@@ -362,8 +366,8 @@ akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q
                                 int32_t max_kv, void *out, void *workspace, size_t workspace_bytes,
                                 akv_stream_t stream);
 
-/* Decode with the step's append fused (one launch for append + decode +
- * split merge): request b's new token -- raw k_new[b] (device [B, Hkv, D]),
+/* Decode with the step's append fused (inside the attention launch):
+ * request b's new token -- raw k_new[b] (device [B, Hkv, D]),
  * v_new[b] -- is written into pool slot new_slot[b] (device int32 [B]),
  * its key rotated at q_pos[b] exactly as akv_append_kv would, before the
  * request's keys are read; kv_indices of request b must end with
@@ -388,9 +392,8 @@ akv_status akv_decode_attention_append(const akv_shape *shape, int32_t B, const 
  * that request's keys are read; request b's index list must then end with
  * new_slot[b] (and its kv_pos entry with q_pos[b]).  Pass all three or none.
  * k_pool/v_pool are written only at those slots.  Workspace: device,
- * 256-byte aligned, akv_decode_rope_workspace() bytes (bf16: split-KV
- * partials and merge counters as for akv_decode_attention; fp32: partials
- * of 512-key chunks).  bf16: keys are rotated in fp32 and rounded to fp16
+ * 256-byte aligned, akv_decode_rope_workspace() bytes (split-KV partials
+ * of 512-key chunks; bf16 adds the merge counters of akv_decode_attention).  bf16: keys are rotated in fp32 and rounded to fp16
  * for the score product, so a rotated key component must stay below 65504
  * in magnitude (a larger one becomes inf); the query keeps ~22 bits as fp16
  * hi + lo parts. */
@@ -436,8 +439,9 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
  *  - Sharing: every call on a device uses the same array.  Calls that
  *    overlap on the GPU (other streams, other host threads) race and corrupt
  *    each other's results; serialise them.  The array keeps the last call's
- *    contents; the call itself clears the merge counters (a memset on
- *    `stream`) and writes every partial it later reads. */
+ *    contents; the call writes every partial it later reads (and, for
+ *    head counts other than 4 and 8, first clears the merge counters with a
+ *    memset on `stream`). */
 akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
                                        const int32_t *q_pos, const void *k_pool,
                                        const void *v_pool, const int32_t *kv_indptr,
