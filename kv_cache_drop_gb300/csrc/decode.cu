@@ -593,23 +593,27 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 }
 
 // ---------------------------------------------------------------------------
-// bf16 decode with rotation on read, all KV heads of a key chunk in one CTA.
-// The rotation of a key needs cos/sin of (position x frequency), the same
-// for every KV head; here a CTA takes (key chunk, request) with one warp per
-// KV head (kHkv = 4 or 8 warps), and the CTA fills, one tile ahead, a shared
-// table of the 16 x 32 cos/sin pairs of each 16-key tile, which every head's
-// warp then reads.  A thread's share of the next table is computed into
-// registers in the middle of the current tile's arithmetic and stored after
-// it, so the sin/cos latency overlaps that work; one barrier per tile then
-// publishes the table and frees the previous one.  The per-head work is the
-// per-head kernel's: 16-key tiles gathered by cp.async (the warps together
-// read a key's whole K and V rows), keys rotated in fp32 and rounded to
-// fp16, the query split into fp16 hi + lo, S in fp16 MMAs, online softmax,
-// P.V in bf16.  Each CTA leaves its chunk's partial (m, l, o) per query
-// head; a second launch merges them (decode_merge_heads_kernel): merged in
-// this kernel by the last CTA of a request, the whole request's merge (all
-// its query heads over all its chunks) ran in one CTA at the end of the
-// launch and made the step 12 % slower.
+// bf16 decode with 4 or 8 KV heads: all KV heads of a key chunk in one CTA.
+// A CTA takes (key chunk, request) with one warp per KV head (kHkv warps),
+// so the CTA reads a key's whole K and V rows.  Per head the work is the
+// per-head kernel's: 16-key tiles gathered by cp.async, the query split
+// into hi + lo parts, S in m16n8k16 MMAs, online softmax, P.V in bf16.
+// kRope (rotation on read): a key's rotation needs cos/sin of (position x
+// frequency), the same for every KV head, so the CTA fills, one tile ahead,
+// a shared table of the 16 x 32 cos/sin pairs of each 16-key tile, which
+// every head's warp then reads.  A thread's share of the next table is
+// computed into registers in the middle of the current tile's arithmetic
+// and stored after it, so the sin/cos latency overlaps that work; one
+// barrier per tile publishes the table and frees the previous one.  Keys
+// are rotated in fp32 (packed over frequency pairs) and rounded to fp16;
+// the query parts and the score MMAs are fp16.  Without kRope (pre-rotated
+// pool) the warps run independently: bf16 query parts and score MMAs, no
+// table, no barrier in the loop.
+// Each CTA leaves its chunk's partial (m, l, o) per query head and a
+// second launch merges them (decode_merge_heads_kernel).  Merged in this
+// kernel by the last CTA of a request, each request's merge (all its query
+// heads over all its chunks) ran in one CTA at the end of the launch and
+// made the rotate-on-read step 12 % slower.
 // ---------------------------------------------------------------------------
 constexpr int kHStages = 2;  // K/V tiles in flight per warp (incl. the one in use)
 // table row of one key: 32 (cos, sin) pairs padded to 40 so that the two
@@ -673,12 +677,13 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
 #pragma unroll
     for (int j = 0; j < kFpt / 2; ++j) {
       const int f = tf + 2 * j;
+      // (cos f, cos f+1, sin f, sin f+1): the rotation's packed operands
       if (wide) {
         const float2 a = rope_cs_wide(thd[f], pos), c = rope_cs_wide(thd[f + 1], pos);
-        cs4[j] = make_float4(a.x, a.y, c.x, c.y);
+        cs4[j] = make_float4(a.x, c.x, a.y, c.y);
       } else {
-        rope_cs_fast(ts.hi[f], ts.lo[f], pos, &cs4[j].x, &cs4[j].y);
-        rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &cs4[j].z, &cs4[j].w);
+        rope_cs_fast(ts.hi[f], ts.lo[f], pos, &cs4[j].x, &cs4[j].z);
+        rope_cs_fast(ts.hi[f + 1], ts.lo[f + 1], pos, &cs4[j].y, &cs4[j].w);
       }
     }
   };
@@ -844,15 +849,17 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
         for (int r = 0; r < 4; ++r) {  // r: (key half, dim half) = (r >> 1, r & 1)
           const int key = gid + 8 * (r >> 1);
           const int f = ks * 16 + 8 * (r & 1) + 2 * tig;
+          // packed over the pair (f, f + 1): y1 = x1 c - x2 s, y2 = x1 s + x2 c
           const float4 t = *reinterpret_cast<const float4 *>(tab + key * kTabRow + f);
-          __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks][r]);
-          __nv_bfloat162 bq = *reinterpret_cast<__nv_bfloat162 *>(&kb[ks + 2][r]);
-          const float x1a = __low2float(a), x1b = __high2float(a);
-          const float x2a = __low2float(bq), x2b = __high2float(bq);
-          const float y1a = x1a * t.x - x2a * t.y, y1b = x1b * t.z - x2b * t.w;
-          const float y2a = x1a * t.y + x2a * t.x, y2b = x1b * t.w + x2b * t.z;
-          kb[ks][r] = pack_f16(y1a, y1b);
-          kb[ks + 2][r] = pack_f16(y2a, y2b);
+          const float2 c = make_float2(t.x, t.y), sn2 = make_float2(t.z, t.w);
+          const float2 nsn = make_float2(-t.z, -t.w);
+          const uint32_t ua = kb[ks][r], ub = kb[ks + 2][r];  // bf16 pairs (f, f + 1)
+          const float2 x1 = make_float2(__uint_as_float(ua << 16), __uint_as_float(ua & 0xffff0000u));
+          const float2 x2 = make_float2(__uint_as_float(ub << 16), __uint_as_float(ub & 0xffff0000u));
+          const float2 y1 = __ffma2_rn(x1, c, __fmul2_rn(x2, nsn));
+          const float2 y2 = __ffma2_rn(x1, sn2, __fmul2_rn(x2, c));
+          kb[ks][r] = pack_f16(y1.x, y1.y);
+          kb[ks + 2][r] = pack_f16(y2.x, y2.y);
         }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
