@@ -615,7 +615,11 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 // heads over all its chunks) ran in one CTA at the end of the launch and
 // made the rotate-on-read step 12 % slower.
 // ---------------------------------------------------------------------------
-constexpr int kHStages = 2;  // K/V tiles in flight per warp (incl. the one in use)
+// K/V tiles per warp (the one in use and those in flight): rotation on read
+// (issue-bound; a third stage measured no faster) and pre-rotated pools
+// (gather-bound; the third stage is 1.6 % faster)
+constexpr int kHStages = 2;
+constexpr int kHStagesPre = 3;
 // table row of one key: 32 (cos, sin) pairs padded to 40 so that the two
 // keys read by one 8-lane phase of a 16-byte load fall in different banks
 constexpr int kTabRow = kD / 2 + 8;
@@ -641,8 +645,9 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
   constexpr int kThreads = kHkv * 32;
   constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
   constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (2 or 4)
+  constexpr int kSt = kRope ? kHStages : kHStagesPre;
   constexpr int kSB = 4096;                   // one stage: K tile 2 KiB | V tile 2 KiB
-  // dynamic smem: [warp][kHStages][stage], then (kRope) two cos/sin tables
+  // dynamic smem: [warp][kSt][stage], then (kRope) two cos/sin tables
   // [16 keys][kTabRow] float2
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float cs[kD / 2], sn[kD / 2];
@@ -663,7 +668,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
         out[(int64_t)b * Hq * kD + i] = __float2bfloat16_rn(0.f);
     return;
   }
-  float2 *tabs = reinterpret_cast<float2 *>(smem + kHkv * kHStages * kSB);
+  float2 *tabs = reinterpret_cast<float2 *>(smem + kHkv * kSt * kSB);
   const int nk = c1 - c0;
   const int n_tiles = (nk + kTileKeys - 1) / kTileKeys;
   // this thread's table entries: key tkey of the tile, frequencies tf..tf+kFpt-1
@@ -732,7 +737,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
     store_tab(0, c4);
   }
 
-  uint8_t *wsm = smem + g * kHStages * kSB;
+  uint8_t *wsm = smem + g * kSt * kSB;
   const uint32_t wsm_u = smem_u32(wsm);
   // pool slot of key `lane` of tile t (0 past the end), loaded one tile
   // ahead of its use
@@ -741,7 +746,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
     return lane < kTileKeys && k < nk ? __ldg(indices + beg + c0 + k) : 0;
   };
   auto issue = [&](int t, int slot) {
-    const int stage = t % kHStages;
+    const int stage = t % kSt;
     if (t < n_tiles) {
       const int k0 = t * kTileKeys;
 #pragma unroll
@@ -759,7 +764,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
   };
   int slot_nx = load_slot(0);
 #pragma unroll
-  for (int t = 0; t < kHStages - 1; ++t) {
+  for (int t = 0; t < kSt - 1; ++t) {
     const int sl = slot_nx;
     slot_nx = load_slot(t + 1);
     issue(t, sl);
@@ -824,12 +829,12 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
 
   for (int it = 0; it < n_tiles; ++it) {
     const int sl = slot_nx;
-    slot_nx = load_slot(it + kHStages);
-    issue(it + kHStages - 1, sl);
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(kHStages - 1));
+    slot_nx = load_slot(it + kSt);
+    issue(it + kSt - 1, sl);
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kSt - 1));
     __syncwarp();
     const float2 *tab = tabs + (it & 1) * (kTileKeys * kTabRow);
-    const uint32_t kt = wsm_u + (it % kHStages) * kSB, vt = kt + 2048;
+    const uint32_t kt = wsm_u + (it % kSt) * kSB, vt = kt + 2048;
     const int k0 = it * kTileKeys;
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
@@ -1294,7 +1299,7 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
     while (n_splits(max_kv, rc) > kMaxSplits) rc *= 2;
     const int rns = n_splits(max_kv, rc);
     Partials rpart = partials(ws, B, Hq, max_kv, rc);
-    const int rsmem = Hkv * kHStages * 4096 + (rope ? 2 * kTabBytes : 0);
+    const int rsmem = Hkv * (rope ? kHStages : kHStagesPre) * 4096 + (rope ? 2 * kTabBytes : 0);
     auto kern = rope ? (Hkv == 8 ? decode_heads_kernel<8, true> : decode_heads_kernel<4, true>)
                      : (Hkv == 8 ? decode_heads_kernel<8, false> : decode_heads_kernel<4, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);
