@@ -494,13 +494,15 @@ def test_decode_rope_more_than_eight_kv_heads():
                      "bf16")
 
 
+@pytest.mark.parametrize("rope", [True, False])
 @pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 8), (16, 4)])
-def test_decode_rope_even_split_edges(Hq, Hkv):
-    """Rotation on read with 4 or 8 KV heads (the kernel that splits the
-    step's entries evenly over one wave of CTAs): requests with no entry, one
-    entry, 15/16/17 entries (tile edges), many short requests sharing a CTA's
-    range, two long ones spanning many CTAs, positions past 2^18 and a
-    negative one; no fused append."""
+def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
+    """4 or 8 KV heads (one CTA per key chunk takes all KV heads; the chunk
+    partials are merged by a dependent launch), with rotation on read or
+    over a pre-rotated pool: requests with no entry, one entry, 15/16/17
+    entries (tile edges), many short requests, two long ones cut into many
+    chunks, positions past 2^18 and a negative one; no fused append; two
+    calls in a row on one workspace."""
     torch = _torch()
     rng = np.random.default_rng(41)
     lens = [0, 1, 15, 16, 17, 0, 5000, 3, 2, 1, 0, 33, 64, 9000, 0, 7] + \
@@ -523,25 +525,32 @@ def test_decode_rope_even_split_edges(Hq, Hkv):
     kvpos = np.concatenate(pos).astype(np.int32)
     max_kv = max(lens)
     out = torch.full((B, Hq, 64), 7.0, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(akv.akv_decode_rope_workspace(shp, B, max_kv), dtype=torch.uint8,
-                     device="cuda")
+    wsb = (akv.akv_decode_rope_workspace if rope else akv.akv_decode_workspace)(shp, B, max_kv)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     kp, vp = akv.to_device(kpool, "bf16"), akv.to_device(vpool, "bf16")
-    for _ in range(2):  # the merge counters are left at zero for the next call
-        akv.akv_decode_attention_rope(shp, B, akv.to_device(q, "bf16"), akv.i32_device(qpos),
-                                      None, None, None, kp, vp, akv.i32_device(indptr),
-                                      akv.i32_device(idx), akv.i32_device(kvpos), max_kv, out, ws)
+    ref = np.zeros((B, Hq, 64))
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        sl = idx[indptr[b]:indptr[b + 1]]
+        kk = oracle.widen(kpool[sl], "bf16")
+        if rope:  # the pool holds raw keys, rotated at their entries' positions
+            kk = oracle.rope(kk, pos[b][:, None], 10000.0)
+        ref[b] = oracle.decode_attention(oracle.widen(q[b:b + 1], "bf16"),
+                                         np.array([qpos[b]]), kk,
+                                         oracle.widen(vpool[sl], "bf16"),
+                                         np.array([0, n]), np.arange(n), "f64", 10000.0)[0]
+    for _ in range(2):  # the workspace is reused as it stands
+        args = (shp, B, akv.to_device(q, "bf16"), akv.i32_device(qpos))
+        if rope:
+            akv.akv_decode_attention_rope(*args, None, None, None, kp, vp, akv.i32_device(indptr),
+                                          akv.i32_device(idx), akv.i32_device(kvpos), max_kv,
+                                          out, ws)
+        else:
+            akv.akv_decode_attention(*args, kp, vp, akv.i32_device(indptr), akv.i32_device(idx),
+                                     max_kv, out, ws)
         torch.cuda.synchronize()
         got = out.float().cpu().numpy()
-        ref = np.zeros((B, Hq, 64))
-        for b, n in enumerate(lens):
-            if n == 0:
-                continue
-            sl = idx[indptr[b]:indptr[b + 1]]
-            kr = oracle.rope(oracle.widen(kpool[sl], "bf16"), pos[b][:, None], 10000.0)
-            ref[b] = oracle.decode_attention(oracle.widen(q[b:b + 1], "bf16"),
-                                             np.array([qpos[b]]), kr,
-                                             oracle.widen(vpool[sl], "bf16"),
-                                             np.array([0, n]), np.arange(n), "f64", 10000.0)[0]
         assert_close(got, ref, "bf16")
         assert not np.any(got[np.array(lens) == 0])  # no entries: zeros
 

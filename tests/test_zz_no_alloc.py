@@ -30,16 +30,19 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _inputs(dtype, seed):
-    dw = workloads.decode_workload(seed=seed, B=3, active=(1500, 7000), steps=2, Hq=16, Hkv=2,
+def _inputs(dtype, seed, Hq=16, Hkv=2):
+    dw = workloads.decode_workload(seed=seed, B=3, active=(1500, 7000), steps=2, Hq=Hq, Hkv=Hkv,
                                    dtype=dtype)
     return dw
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_static_decode_matches_workspace_decode(dtype):
+# (16, 2): the per-head kernel, merge in the launch; (64, 8), (16, 4): the
+# all-heads kernel and its dependent merge launch
+@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 16, 2), ("bf16", 64, 8), ("bf16", 16, 4),
+                                          ("f32", 16, 2)])
+def test_static_decode_matches_workspace_decode(dtype, Hq, Hkv):
     import torch
-    dw = _inputs(dtype, 21)
+    dw = _inputs(dtype, 21, Hq, Hkv)
     shp = akv.shape(dw.Hq, dw.Hkv, 64, dtype)
     kp = akv.to_device(dw.k_pool, dtype)
     vp = akv.to_device(dw.v_pool, dtype)
@@ -70,13 +73,14 @@ def test_static_decode_matches_workspace_decode(dtype):
         assert_close(got.float().cpu().numpy(), want, dtype)
 
 
-def test_static_decode_allocates_nothing():
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (64, 8)])
+def test_static_decode_allocates_nothing(Hq, Hkv):
     """After a first call (which may load the module holding the array), more
     calls leave the device's free memory exactly where it was; a call with
     B = 0 is accepted (set-up only)."""
     import torch
     dtype = "bf16"
-    dw = _inputs(dtype, 23)
+    dw = _inputs(dtype, 23, Hq, Hkv)
     shp = akv.shape(dw.Hq, dw.Hkv, 64, dtype)
     kp = akv.to_device(dw.k_pool, dtype)
     vp = akv.to_device(dw.v_pool, dtype)
