@@ -504,10 +504,11 @@ def decode_part(dw, warmup_steps=8):
     torch.cuda.empty_cache()
     return dict(B=dw.B, steps=dw.steps, ms_total=ms, ms_per_step=ms / dw.steps,
                 bytes_per_step=bytes_total / dw.steps, gbs=bytes_total / ms / 1e6,
-                active_entries_per_step=n_total / dw.steps, launches_per_step=1,
-                memsets_per_step=1,
+                active_entries_per_step=n_total / dw.steps, launches_per_step=2,
+                memsets_per_step=0,
+                note="attention with the append fused, then the dependent merge launch",
                 separate_calls=dict(ms_per_step=ms_sep / dw.steps,
-                                    gbs=bytes_total / ms_sep / 1e6, launches_per_step=2,
+                                    gbs=bytes_total / ms_sep / 1e6, launches_per_step=3,
                                     note="akv_append_kv + akv_decode_attention"),
                 rotate_on_read=dict(ms_per_step=ms_rope / dw.steps,
                                     bytes_per_step=bytes_rope / dw.steps,
