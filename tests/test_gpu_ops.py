@@ -501,8 +501,8 @@ def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
     partials are merged by a dependent launch), with rotation on read or
     over a pre-rotated pool: requests with no entry, one entry, 15/16/17
     entries (tile edges), many short requests, two long ones cut into many
-    chunks, positions past 2^18 and a negative one; no fused append; two
-    calls in a row on one workspace."""
+    chunks, positions past 2^18 and a negative one, peaky scores for every
+    fourth request; no fused append; two calls in a row on one workspace."""
     torch = _torch()
     rng = np.random.default_rng(41)
     lens = [0, 1, 15, 16, 17, 0, 5000, 3, 2, 1, 0, 33, 64, 9000, 0, 7] + \
@@ -511,7 +511,9 @@ def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
     shp = akv.shape(Hq, Hkv, 64, "bf16")
     kpool = workloads.bf16_bits(rng.standard_normal((S, Hkv, 64)).astype(np.float32))
     vpool = workloads.bf16_bits(rng.standard_normal((S, Hkv, 64)).astype(np.float32))
-    q = workloads.bf16_bits(rng.standard_normal((B, Hq, 64)).astype(np.float32))
+    qf = rng.standard_normal((B, Hq, 64)).astype(np.float32)
+    qf[1::4] *= 8  # peaky scores (std ~ 8) for every fourth request
+    q = workloads.bf16_bits(qf)
     indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     idx = rng.integers(0, S, size=int(indptr[-1])).astype(np.int32)
     pos, qpos = [], []
