@@ -636,12 +636,11 @@ __device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
 template <int kHkv, bool kRope>
 __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
     decode_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
-                             const int32_t *__restrict__ qpos, __nv_bfloat16 *kp,
-                             __nv_bfloat16 *vp, const int32_t *__restrict__ indptr,
-                             const int32_t *__restrict__ indices, Partials part, RopeTheta th,
-                             __nv_bfloat16 *out, const __nv_bfloat16 *k_new,
-                             const __nv_bfloat16 *v_new, const int32_t *new_slot, int chunk,
-                             const int32_t *__restrict__ kvpos) {
+                        const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
+                        const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                        Partials part, RopeTheta th, __nv_bfloat16 *out,
+                        const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                        const int32_t *new_slot, int chunk, const int32_t *__restrict__ kvpos) {
   constexpr int kThreads = kHkv * 32;
   constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
   constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (2 or 4)

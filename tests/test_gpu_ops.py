@@ -249,12 +249,13 @@ def _run_decode_fused(dw, check_steps):
     return results, kp, vp
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_decode_fused_append_equals_separate_calls(dtype):
+# (8, 2): the per-head kernel; (64, 8): the all-heads kernel
+@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 8, 2), ("f32", 8, 2), ("bf16", 64, 8)])
+def test_decode_fused_append_equals_separate_calls(dtype, Hq, Hkv):
     """Append fused into the decode launch: outputs and the pool bit-identical
     to akv_append_kv followed by akv_decode_attention, and close to fp64."""
     torch = _torch()
-    dw = workloads.decode_workload(seed=14, B=3, active=(100, 5000), steps=3, Hq=8, Hkv=2,
+    dw = workloads.decode_workload(seed=14, B=3, active=(100, 5000), steps=3, Hq=Hq, Hkv=Hkv,
                                    dtype=dtype)
     sep = _run_decode(dw, {0, 1, 2})
     fused, kp, vp = _run_decode_fused(dw, {0, 1, 2})
