@@ -518,6 +518,34 @@ def decode_part(dw, warmup_steps=8):
                                          "chunk partials merged by a second launch"))
 
 
+def gemm_part(M, N, K, steps=3):
+    """One projection GEMM of the decoder (akv_gemm_bf16, bf16 out) alone, at
+    M rows: the FFN up projection of the 4-layer decoder is M = 1,048,576,
+    N = 4096, K = 1024; smaller M only for profiling captures."""
+    import torch
+    import kv_cache_drop_gb300 as akv
+    g = torch.Generator(device="cuda").manual_seed(5)
+    a = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn((N, K), device="cuda", generator=g) * K ** -0.5).to(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    akv.akv_gemm_bf16(M, N, K, a, w, y, 0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        akv.akv_gemm_bf16(M, N, K, a, w, y, 0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pk = peaks()
+    tf = 2 * M * N * K / ms / 1e9
+    del a, w, y
+    torch.cuda.empty_cache()
+    return dict(M=M, N=N, K=K, ms=ms, tflops=tf, frac_of_measured_burst=tf / pk["bf16"],
+                frac_of_measured_sustained=tf / pk["bf16_sus"])
+
+
 def decoder_part(mw, steps=3):
     """The 4-layer decoder restoration (32 requests sharing a prefix): whole
     forward, plus its segment attention and FFN GEMM timed alone."""
@@ -725,9 +753,11 @@ def run_ours(args, rank, world):
     import workloads
     akv.lib()
     pk = peaks()
-    if args.part in ("repos", "decode", "decoder", "tree"):  # one secondary workload alone
+    if args.part in ("repos", "decode", "decoder", "tree", "gemm"):  # one workload alone
         if args.part == "tree":
             res = tree_part()
+        elif args.part == "gemm":
+            res = gemm_part(args.gemm_m, 4096, 1024, max(1, args.steps))
         elif args.part == "repos":
             res = repos_part(workloads.repos_config(), args.steps, args.warmup)
             res["batch"] = repos_batch_part(workloads.decode_workload(), args.steps, args.warmup)
@@ -886,8 +916,10 @@ def main():
                          "workload; fewer only for small profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--part", default="all",
-                    choices=["all", "repos", "decode", "decoder", "tree"],
+                    choices=["all", "repos", "decode", "decoder", "tree", "gemm"],
                     help="run one secondary workload alone (for profiling captures)")
+    ap.add_argument("--gemm-m", type=int, default=1 << 20,
+                    help="rows of the --part gemm projection (N = 4096, K = 1024)")
     args = ap.parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

@@ -10,6 +10,16 @@
 // fp32 output (the residual stream) or apply SwiGLU, while the next tile
 // accumulates into the other one.  Waits are bounded like the attention
 // kernel's.
+//
+// CTAs run in clusters of two that work on vertically adjacent tiles (the
+// same 256 W rows, M tiles 2i and 2i + 1): each CTA loads its own X block
+// and one half of the W block, which TMA multicasts into both CTAs' shared
+// memory, so a K block costs each SM 32 KB of L2 reads instead of 48.  At
+// one CTA per SM the K-block ring bounds the bytes in flight, and without
+// the multicast the L2-to-SM stream (about 27 TB/s of L2 reads at full
+// tensor rate) held the tensor pipe near 65% busy.  A stage of a CTA is
+// refilled only after both CTAs' MMAs have read it: each MMA commit
+// arrives on the stage's "empty" barrier in both CTAs.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -20,7 +30,9 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
 constexpr int kThreads = 192;
+constexpr int kCluster = 2;  // CTAs per cluster (two M tiles sharing each W block)
 constexpr uint32_t kABytes = BM * BK * 2, kBBytes = BN * BK * 2;
+constexpr uint32_t kBPartBytes = kBBytes / kCluster;  // the W rows one CTA loads
 constexpr long long kWaitBudget = 1000000000LL;
 
 struct __align__(1024) GemmSmem {
@@ -33,6 +45,37 @@ struct __align__(1024) GemmSmem {
 
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, uint32_t *status) {
   ptx::mbar_wait_grid(bar, parity, status, kStatusWaitTimeout, kWaitBudget);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of both CTAs: release this CTA's earlier writes (barrier
+// initialisation) to the peer, and wait until the peer has arrived too
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// TMA 2D load whose box is written at the same shared-memory offset in
+// every CTA of `mask`, each signalling its own mbarrier at `bar`'s offset
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
+                                               int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(ptx::smem_addr(dst)),
+      "l"((uint64_t)m), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+// once the MMAs issued before it have completed, arrive on the mbarrier at
+// `bar`'s offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(ptx::smem_addr(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 // Epilogue of one 128 x 256 tile: this thread's row of the accumulator at
@@ -113,24 +156,33 @@ __device__ __forceinline__ void store_tile(uint32_t tl, int m, int n0, int M, in
   }
 }
 
-// Persistent: CTA c takes output tiles c, c + gridDim.x, ... (row-major over
-// the tile grid, so consecutive tiles share their X rows).  The K-block ring
-// runs on across tiles; TMEM holds two 256-column accumulators, so the
-// epilogue warps drain tile j while the MMA thread computes tile j + 1.
-__global__ void __launch_bounds__(kThreads, 1)
+// Persistent: cluster q takes tile pairs q, q + clusters, ... (row-major over
+// the grid of (M tile pair, N tile), so consecutive pairs share their X
+// rows); rank r of the cluster computes M tile 2i + r of pair (i, n).  A
+// pair whose second M tile lies past M still runs in full (its X rows are
+// read as zeros, its rows are not stored), so both CTAs issue the same
+// loads.  The K-block ring runs on across tiles; TMEM holds two 256-column
+// accumulators, so the epilogue warps drain tile j while the MMA thread
+// computes tile j + 1.
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int M, int N, int K, void *__restrict__ Y, int out_mode, uint32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem &sm = *reinterpret_cast<GemmSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();
+  const int q0 = blockIdx.x / kCluster, nq = gridDim.x / kCluster;
   const int nk = (K + BK - 1) / BK;
   const int tiles_n = (N + BN - 1) / BN;
-  const int n_tiles = tiles_n * ((M + BM - 1) / BM);
+  const int n_tiles = tiles_n * ((M + kCluster * BM - 1) / (kCluster * BM));  // tile groups
+  // tile pair t: rows of this CTA's M tile, first column of its N tile
+  auto m0_of = [&](int t) { return ((t / tiles_n) * kCluster + rank) * BM; };
+  auto n0_of = [&](int t) { return (t % tiles_n) * BN; };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
-      ptx::mbar_init(&sm.empty[s], 1);
+      ptx::mbar_init(&sm.empty[s], kCluster);  // both CTAs' MMAs have read the stage
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sm.acc_full[b], 1);
@@ -143,25 +195,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  cluster_sync();  // the peer's barriers exist before any multicast or remote arrive
 
   if (warp == 0) {
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmA);
       ptx::tma_prefetch_desc(&tmB);
       int c = 0;  // K blocks loaded so far, over all tiles
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      for (int t = q0; t < n_tiles; t += nq) {
+        const int m0 = m0_of(t), n0 = n0_of(t);
         for (int kb = 0; kb < nk; ++kb, ++c) {
           const int s = c % kStages;
           if (c >= kStages) wait_bar(&sm.empty[s], ((c / kStages) - 1) & 1, status);
+          // this CTA's X block, and its half of the W block into both CTAs
           ptx::mbar_expect_tx(&sm.full[s], kABytes + kBBytes);
           ptx::tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * BK, m0);
-          ptx::tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * BK, n0);
+          tma_load_2d_mc(sm.b[s] + rank * kBPartBytes, &tmB, &sm.full[s], kb * BK,
+                         n0 + rank * (BN / kCluster), (uint16_t)((1u << kCluster) - 1));
         }
       }
-      // every copy has landed before the CTA exits
-      for (int c2 = c > kStages ? c - kStages : 0; c2 < c; ++c2)
+      // before the CTA exits: every copy into it has landed (its own and the
+      // peer's multicasts), and both CTAs' last MMA commits have arrived here
+      for (int c2 = c > kStages ? c - kStages : 0; c2 < c; ++c2) {
         wait_bar(&sm.full[c2 % kStages], (c2 / kStages) & 1, status);
+        wait_bar(&sm.empty[c2 % kStages], (c2 / kStages) & 1, status);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -170,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t db = ptx::sdesc_sw128(ptx::smem_addr(sm.b[0]));
       int c = 0;
       int j = 0;  // this CTA's tile count
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+      for (int t = q0; t < n_tiles; t += nq, ++j) {
         const int acc = j & 1;
         // accumulator acc was last used by tile j - 2: wait until drained
         if (j >= 2) wait_bar(&sm.acc_empty[acc], ((j >> 1) - 1) & 1, status);
@@ -184,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             ptx::mma_f16_ss(d, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(&sm.empty[s]);
+          mma_commit_mc(&sm.empty[s], (uint16_t)((1u << kCluster) - 1));  // both CTAs' stage s
         }
         ptx::mma_commit(&sm.acc_full[acc]);
       }
@@ -194,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     int j = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+    for (int t = q0; t < n_tiles; t += nq, ++j) {
       const int acc = j & 1;
-      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      const int m0 = m0_of(t), n0 = n0_of(t);
       wait_bar(&sm.acc_full[acc], (j >> 1) & 1, status);
       ptx::tc_fence_after();
       store_tile(tmem + lanes + BN * acc, m0 + row, n0, M, N, Y, out_mode);
@@ -209,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA exits while the other may still write into it
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 2 * BN);
@@ -266,17 +325,25 @@ cudaError_t launch_gemm(int M, int N, int K, const void *x, const void *w, void 
                         uint32_t *status, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, x, M, K, BM) || !make_map(&mb, w, N, K, BN)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, x, M, K, BM) || !make_map(&mb, w, N, K, BN / kCluster))
+    return cudaErrorInvalidValue;
   const int smem = (int)sizeof(GemmSmem) + 1024;
   // per device, so set on every launch (cheap)
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
-  const int64_t n_tiles = (int64_t)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
-  const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
+  // one wave of clusters: as many as can be resident at once (one CTA per
+  // SM; a GPC with an odd SM count leaves one SM out), at most one per pair
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const int64_t n_groups = (int64_t)((N + BN - 1) / BN) * ((M + kCluster * BM - 1) / (kCluster * BM));
+  const unsigned grid = (unsigned)(kCluster * (n_groups < clusters ? n_groups : clusters));
   gemm_kernel<<<grid, kThreads, smem, s>>>(ma, mb, M, N, K, y, out_mode, status);
   return cudaGetLastError();
 }

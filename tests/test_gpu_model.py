@@ -29,10 +29,12 @@ def _bf16(a, dev="cuda"):
 
 @pytest.mark.parametrize("M,N,K", [(300, 352, 200), (128, 256, 64), (1000, 1024, 1024),
                                    (77, 4096, 1024),
-                                   # 65 x 9 = 585 tiles: about four per CTA of the
-                                   # persistent kernel (both accumulators, each reused
-                                   # after its epilogue), ragged last tile row and
-                                   # column, a partial last K block
+                                   # 65 x 9 = 585 tiles, 297 pairs of vertically
+                                   # adjacent tiles: about four per two-CTA cluster of
+                                   # the persistent kernel (both accumulators, each
+                                   # reused after its epilogue), an odd tile count (the
+                                   # last pair's second tile lies past M), ragged last
+                                   # tile row and column, a partial last K block
                                    (8200, 2208, 328)])
 def test_gemm_modes(M, N, K):
     torch = _torch()
