@@ -29,6 +29,9 @@ def _bf16(a, dev="cuda"):
 
 @pytest.mark.parametrize("M,N,K", [(300, 352, 200), (128, 256, 64), (1000, 1024, 1024),
                                    (77, 4096, 1024),
+                                   # one M tile, N of 32 (both W halves mostly or
+                                   # wholly past N), K below one block
+                                   (64, 32, 16), (384, 96, 72),
                                    # 65 x 9 = 585 tiles, 297 pairs of vertically
                                    # adjacent tiles: about four per two-CTA cluster of
                                    # the persistent kernel (both accumulators, each
