@@ -1274,17 +1274,8 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         void *out, void *ws, const RopeTheta &th, const void *k_new,
                         const void *v_new, const int32_t *new_slot, cudaStream_t s,
                         const int32_t *kvpos = nullptr) {
-  // chunk: the largest of 4096, 2048, 1024 keys that still gives about two
-  // waves of CTAs (4 per SM) when every request is max_kv long
   const int sms = device_sms();
-  int chunk = kMaxChunk;
-  while (chunk > kMinChunk && (int64_t)B * n_splits(max_kv, chunk) * Hkv < 2LL * 4 * sms) chunk /= 2;
-  while (n_splits(max_kv, chunk) > kMaxSplits) chunk *= 2;
-  const int ns = n_splits(max_kv, chunk);
-  Partials part = partials(ws, B, Hq, max_kv, chunk);
   const bool rope = kvpos != nullptr;
-  int *counters = reinterpret_cast<int *>(
-      static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv, rope));
   if (Hkv == 4 || Hkv == 8) {
     // all KV heads of a chunk in one CTA of Hkv warps (two CTAs per SM for
     // 8 heads, three for 4: shared memory); the chunk is the largest that
@@ -1322,6 +1313,16 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
     return cudaLaunchKernelEx(&cfg, decode_merge_heads_kernel, Hq, rns, rc, indptr, rpart,
                               (__nv_bfloat16 *)out);
   }
+  // other head counts: a CTA per (chunk, KV head, request); the chunk is the
+  // largest of 4096, 2048, 1024 keys that still gives about two waves of
+  // CTAs (4 per SM) when every request is max_kv long
+  int chunk = kMaxChunk;
+  while (chunk > kMinChunk && (int64_t)B * n_splits(max_kv, chunk) * Hkv < 2LL * 4 * sms) chunk /= 2;
+  while (n_splits(max_kv, chunk) > kMaxSplits) chunk *= 2;
+  const int ns = n_splits(max_kv, chunk);
+  Partials part = partials(ws, B, Hq, max_kv, chunk);
+  int *counters = reinterpret_cast<int *>(
+      static_cast<char *>(ws) + decode_partials_bytes(B, Hq, max_kv, rope));
   // dynamic shared memory: the tile buffers, or the merge's per-split
   // weights ([16 rows][ns] floats and 16 row totals) when those are larger
   const int smem = std::max(kWarps * kStages * kStageBytes(rope), (16 * ns + 16) * 4);
