@@ -418,6 +418,31 @@ def repos_batch_part(dw, steps, warmup):
                 note="inputs (1.7 GB pool + 1.6 GB written) exceed L2; no flush needed")
 
 
+def graph_steps_ms(run_all, stream):
+    """Capture run_all() (a sequence of library calls on the current stream)
+    as one CUDA graph, replay it once untimed and once timed: device ms."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):  # the calls' first-use set-up, outside the capture
+        run_all()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_all()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    del g
+    return ms
+
+
 def decode_part(dw, warmup_steps=8):
     import torch
     import kv_cache_drop_gb300 as akv
@@ -458,6 +483,9 @@ def decode_part(dw, warmup_steps=8):
         ev[s + 1].record(stream)
     torch.cuda.synchronize()
     per_step = [ev[s].elapsed_time(ev[s + 1]) for s in range(dw.steps)]
+    # the same steps captured as one CUDA graph (every step's inputs are its
+    # own device tensors, so the graph needs no copies) and replayed
+    ms_graph = graph_steps_ms(lambda: [one(st) for st in steps], stream)
     # the same steps as two calls (akv_append_kv, akv_decode_attention)
     ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(dw.steps + 1)]
     ev2[0].record(stream)
@@ -499,6 +527,7 @@ def decode_part(dw, warmup_steps=8):
         ev[s + 1].record(stream)
     torch.cuda.synchronize()
     ms_rope = float(np.sum([ev[s].elapsed_time(ev[s + 1]) for s in range(dw.steps)]))
+    ms_rope_graph = graph_steps_ms(lambda: [one_rope(st) for st in steps], stream)
     bytes_rope = bytes_total + 4 * n_total  # + one position per entry
     del kp, vp, ws, wsr, steps
     torch.cuda.empty_cache()
@@ -507,6 +536,8 @@ def decode_part(dw, warmup_steps=8):
                 active_entries_per_step=n_total / dw.steps, launches_per_step=2,
                 memsets_per_step=0,
                 note="attention with the append fused, then the dependent merge launch",
+                graph=dict(ms_per_step=ms_graph / dw.steps, gbs=bytes_total / ms_graph / 1e6,
+                           note="the 256 steps captured as one CUDA graph, replayed once"),
                 separate_calls=dict(ms_per_step=ms_sep / dw.steps,
                                     gbs=bytes_total / ms_sep / 1e6, launches_per_step=3,
                                     note="akv_append_kv + akv_decode_attention"),
@@ -514,6 +545,7 @@ def decode_part(dw, warmup_steps=8):
                                     bytes_per_step=bytes_rope / dw.steps,
                                     gbs=bytes_rope / ms_rope / 1e6, launches_per_step=2,
                                     memsets_per_step=0,
+                                    graph_ms_per_step=ms_rope_graph / dw.steps,
                                     note="raw-key pool, per-entry positions, append fused; "
                                          "chunk partials merged by a second launch"))
 

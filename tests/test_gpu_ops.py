@@ -558,6 +558,78 @@ def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
         assert not np.any(got[np.array(lens) == 0])  # no entries: zeros
 
 
+@pytest.mark.parametrize("rope", [False, True])
+def test_decode_steps_in_a_cuda_graph(rope):
+    """A serving step (decode with the append fused, GQA 64/8: the all-heads
+    kernel and its dependent merge launch) captured once in a CUDA graph and
+    replayed for three steps, each step's inputs copied into the captured
+    buffers first: outputs and pools equal the same steps called eagerly,
+    bit for bit."""
+    torch = _torch()
+    dw = workloads.decode_workload(seed=51, B=4, active=(2000, 9000), steps=3, Hq=64, Hkv=8)
+    shp = akv.shape(dw.Hq, dw.Hkv, 64, "bf16")
+    max_kv = max(len(a) for a in dw.active_slots) + dw.steps
+    pos_act = _rope_positions(dw, seed=52)
+    wsb = (akv.akv_decode_rope_workspace if rope else akv.akv_decode_workspace)(shp, dw.B, max_kv)
+
+    def inputs(step):
+        indptr, idx = dw.indices_at(step)
+        kvpos = np.concatenate([np.concatenate([pos_act[b], dw.L[b] + np.arange(step + 1)])
+                                for b in range(dw.B)]).astype(np.int32)
+        qpos = dw.L + step
+        return dict(q=akv.to_device(dw.q[step], "bf16"), pos=akv.i32_device(qpos),
+                    kn=akv.to_device(dw.k_new[step], "bf16"),
+                    vn=akv.to_device(dw.v_new[step], "bf16"),
+                    slots=akv.i32_device(dw.append_slots[step]), indptr=akv.i32_device(indptr),
+                    idx=akv.i32_device(idx), kvpos=akv.i32_device(kvpos))
+
+    def step_call(t, kp, vp, out, ws):
+        if rope:
+            akv.akv_decode_attention_rope(shp, dw.B, t["q"], t["pos"], t["kn"], t["vn"],
+                                          t["slots"], kp, vp, t["indptr"], t["idx"], t["kvpos"],
+                                          max_kv, out, ws)
+        else:
+            akv.akv_decode_attention_append(shp, dw.B, t["q"], t["pos"], t["kn"], t["vn"],
+                                            t["slots"], kp, vp, t["indptr"], t["idx"], max_kv,
+                                            out, ws)
+
+    # eager
+    kp_e, vp_e = akv.to_device(dw.k_pool, "bf16"), akv.to_device(dw.v_pool, "bf16")
+    ws_e = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    eager = []
+    for step in range(dw.steps):
+        out = torch.empty((dw.B, dw.Hq, 64), dtype=torch.bfloat16, device="cuda")
+        step_call(inputs(step), kp_e, vp_e, out, ws_e)
+        eager.append(out)
+    # captured: buffers sized for the last step (the index lists grow by one
+    # entry per request and step; the grid depends only on max_kv)
+    kp_g, vp_g = akv.to_device(dw.k_pool, "bf16"), akv.to_device(dw.v_pool, "bf16")
+    ws_g = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    last = inputs(dw.steps - 1)
+    buf = {k: torch.zeros_like(v) for k, v in last.items()}
+    out_g = torch.empty((dw.B, dw.Hq, 64), dtype=torch.bfloat16, device="cuda")
+
+    def load(step):
+        for k, v in inputs(step).items():
+            buf[k][:v.numel()].copy_(v)
+
+    load(0)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        step_call(buf, kp_g, vp_g, out_g, ws_g)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_call(buf, kp_g, vp_g, out_g, ws_g)
+    for step in range(dw.steps):
+        load(step)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, eager[step]), f"step {step}"
+    assert torch.equal(kp_g, kp_e) and torch.equal(vp_g, vp_e)
+
+
 def test_decode_rope_full_size():
     """14 requests, 20k-90k keys, GQA 64/8 (one CTA reads whole pool rows):
     256 steps with the append fused; steps 0 and 255 checked in full."""
