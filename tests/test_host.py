@@ -137,6 +137,30 @@ def test_workspace_queries_are_host_only(akv):
     assert akv.akv_compact_workspace(r.ops(), r.T) > 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,B,max_kv", [(64, 8, 14, 90000), (16, 4, 3, 1), (8, 2, 1, 0),
+                                            (128, 8, 65535, 2048), (64, 8, 2, 2_048_000)])
+def test_decode_workspace_sizes(akv, Hq, Hkv, B, max_kv):
+    """The decode workspaces as the header states them, on the host alone:
+    split-KV partials ((m, l) pairs, then the rows' outputs: 66 floats per
+    (request, query head, split)) over 1,024-key splits, or 512-key splits
+    with rotation on read, each part rounded up to 256 bytes, then B x Hkv
+    int32 merge counters (bf16); fp32 rotation on read has no counters."""
+    r256 = lambda n: (n + 255) // 256 * 256
+
+    def partials(chunk):
+        ns = 1 if max_kv <= 0 else -(-max_kv // chunk)
+        return r256(B * Hq * ns * 2 * 4) + r256(B * Hq * ns * 64 * 4)
+
+    counters = r256(B * Hkv * 4)
+    for dt in ("bf16", "f32"):
+        shp = akv.shape(Hq, Hkv, 64, dt)
+        assert akv.akv_decode_workspace(shp, B, max_kv) == partials(1024) + counters
+    assert akv.akv_decode_rope_workspace(akv.shape(Hq, Hkv, 64, "bf16"), B, max_kv) == \
+        partials(512) + counters
+    assert akv.akv_decode_rope_workspace(akv.shape(Hq, Hkv, 64, "f32"), B, max_kv) == \
+        partials(512)
+
+
 INVALID, UNSUPPORTED = 1, 4
 
 
