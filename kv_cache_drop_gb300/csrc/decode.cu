@@ -634,7 +634,7 @@ __device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
 }
 
 template <int kHkv, bool kRope>
-__global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : 3)
+__global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
     decode_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
                         const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
                         const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
@@ -1276,12 +1276,15 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         const int32_t *kvpos = nullptr) {
   const int sms = device_sms();
   const bool rope = kvpos != nullptr;
-  if (Hkv == 4 || Hkv == 8) {
+  // 4 or 8 KV heads, and 2 over a pre-rotated pool (with rotation on read a
+  // 2-warp CTA spreads each tile's angle table over too few threads: 5%
+  // slower than the per-head kernel there, and 22% faster without it)
+  if (Hkv == 4 || Hkv == 8 || (Hkv == 2 && !rope)) {
     // all KV heads of a chunk in one CTA of Hkv warps (two CTAs per SM for
-    // 8 heads, three for 4: shared memory); the chunk is the largest that
-    // still gives about kHeadsWaves waves of CTAs when every request is
-    // max_kv long; then the merge launch
-    const int per_sm = Hkv == 8 ? 2 : 3;
+    // 8 heads, three for 4: shared memory, eight for 2); the chunk is the
+    // largest that still gives about kHeadsWaves waves of CTAs when every
+    // request is max_kv long; then the merge launch
+    const int per_sm = Hkv == 8 ? 2 : Hkv == 4 ? 3 : 8;
     int rc = kMaxChunk;
     const int floor = rope ? kRChunk : kMinChunk;  // the workspace holds that many splits
     while (rc > floor && (int64_t)B * n_splits(max_kv, rc) < (int64_t)kHeadsWaves * per_sm * sms)
@@ -1291,7 +1294,9 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
     Partials rpart = partials(ws, B, Hq, max_kv, rc);
     const int rsmem = Hkv * (rope ? kHStages : kHStagesPre) * 4096 + (rope ? 2 * kTabBytes : 0);
     auto kern = rope ? (Hkv == 8 ? decode_heads_kernel<8, true> : decode_heads_kernel<4, true>)
-                     : (Hkv == 8 ? decode_heads_kernel<8, false> : decode_heads_kernel<4, false>);
+                     : (Hkv == 8   ? decode_heads_kernel<8, false>
+                        : Hkv == 4 ? decode_heads_kernel<4, false>
+                                   : decode_heads_kernel<2, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);
     if (e != cudaSuccess) return e;
     kern<<<dim3(rns, B), Hkv * 32, rsmem, s>>>(

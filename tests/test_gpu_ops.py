@@ -249,8 +249,9 @@ def _run_decode_fused(dw, check_steps):
     return results, kp, vp
 
 
-# (8, 2): the per-head kernel; (64, 8): the all-heads kernel
-@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 8, 2), ("f32", 8, 2), ("bf16", 64, 8)])
+# (8, 1): the per-head kernel; (8, 2), (64, 8): the all-heads kernel
+@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 8, 1), ("bf16", 8, 2), ("f32", 8, 2),
+                                          ("bf16", 64, 8)])
 def test_decode_fused_append_equals_separate_calls(dtype, Hq, Hkv):
     """Append fused into the decode launch: outputs and the pool bit-identical
     to akv_append_kv followed by akv_decode_attention, and close to fp64."""
