@@ -355,10 +355,10 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
  * host, an upper bound on any request's length (sizes the split-KV grid).
  * out [B, Hq, D] device.  A request with no keys gets zeros.
  * Limits: B <= 65535; bf16: max_kv <= 2,048,000 (AKV_ERR_UNSUPPORTED).
- * Work on `stream` (bf16): with 2, 4 or 8 KV heads (2 not with rotation on
- * read), the attention launch (one CTA per key chunk and request, all KV
- * heads) and the split merge as a programmatic dependent launch; other head
- * counts, a memset of B x Hkv merge counters and one launch that also
+ * Work on `stream` (bf16): with 4 or 8 KV heads, and 2 or 16 without
+ * rotation on read, the attention launch (one CTA per key chunk and request,
+ * all KV heads) and the split merge as a programmatic dependent launch;
+ * otherwise a memset of B x Hkv merge counters and one launch that also
  * merges. */
 size_t akv_decode_workspace(const akv_shape *shape, int32_t B, int32_t max_kv);
 akv_status akv_decode_attention(const akv_shape *shape, int32_t B, const void *q,
@@ -441,8 +441,8 @@ akv_status akv_decode_attention_rope(const akv_shape *shape, int32_t B, const vo
  *    overlap on the GPU (other streams, other host threads) race and corrupt
  *    each other's results; serialise them.  The array keeps the last call's
  *    contents; the call writes every partial it later reads (and, for
- *    head counts other than 2, 4 and 8, first clears the merge counters
- *    with a memset on `stream`). */
+ *    head counts other than 2, 4, 8 and 16, first clears the merge
+ *    counters with a memset on `stream`). */
 akv_status akv_decode_attention_static(const akv_shape *shape, int32_t B, const void *q,
                                        const int32_t *q_pos, const void *k_pool,
                                        const void *v_pool, const int32_t *kv_indptr,

@@ -634,7 +634,7 @@ __device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
 }
 
 template <int kHkv, bool kRope>
-__global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
+__global__ void __launch_bounds__(kHkv * 32, kHkv == 16 ? 1 : kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
     decode_heads_kernel(int Hq, const __nv_bfloat16 *__restrict__ q,
                         const int32_t *__restrict__ qpos, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
                         const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
@@ -643,7 +643,8 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
                         const int32_t *new_slot, int chunk, const int32_t *__restrict__ kvpos) {
   constexpr int kThreads = kHkv * 32;
   constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
-  constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (2 or 4)
+  constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (kRope: 2 or 4)
+  constexpr int kNc4 = kFpt >= 2 ? kFpt / 2 : 1;  // float4 per thread (16 heads: no table)
   constexpr int kSt = kRope ? kHStages : kHStagesPre;
   constexpr int kSB = 4096;                   // one stage: K tile 2 KiB | V tile 2 KiB
   // dynamic smem: [warp][kSt][stage], then (kRope) two cos/sin tables
@@ -731,7 +732,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
   }
   __syncthreads();  // frequencies staged, the appended row visible
   if (kRope) {
-    float4 c4[kFpt / 2];
+    float4 c4[kNc4];
     angles(pos0, c4);
     store_tab(0, c4);
   }
@@ -881,7 +882,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 8 ? 2 : kHkv == 4 ? 3 : 8)
       }
     }
     // the next tile's angles (stored after this tile's arithmetic)
-    float4 nxt[kFpt / 2];
+    float4 nxt[kNc4];
     if (kRope) {
       angles(pos1, nxt);
       pos1 = pos2;
@@ -1276,15 +1277,16 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         const int32_t *kvpos = nullptr) {
   const int sms = device_sms();
   const bool rope = kvpos != nullptr;
-  // 4 or 8 KV heads, and 2 over a pre-rotated pool (with rotation on read a
-  // 2-warp CTA spreads each tile's angle table over too few threads: 5%
-  // slower than the per-head kernel there, and 22% faster without it)
-  if (Hkv == 4 || Hkv == 8 || (Hkv == 2 && !rope)) {
-    // all KV heads of a chunk in one CTA of Hkv warps (two CTAs per SM for
-    // 8 heads, three for 4: shared memory, eight for 2); the chunk is the
-    // largest that still gives about kHeadsWaves waves of CTAs when every
-    // request is max_kv long; then the merge launch
-    const int per_sm = Hkv == 8 ? 2 : Hkv == 4 ? 3 : 8;
+  // 4 or 8 KV heads, and 2 or 16 over a pre-rotated pool (with rotation on
+  // read a 2-warp CTA spreads each tile's angle table over too few threads:
+  // 5% slower than the per-head kernel there, and 22% faster without it; 16
+  // heads take 512 threads, whose table share would be one frequency each)
+  if (Hkv == 4 || Hkv == 8 || ((Hkv == 2 || Hkv == 16) && !rope)) {
+    // all KV heads of a chunk in one CTA of Hkv warps (one CTA per SM for 16
+    // heads, two for 8, three for 4: shared memory, eight for 2); the chunk
+    // is the largest that still gives about kHeadsWaves waves of CTAs when
+    // every request is max_kv long; then the merge launch
+    const int per_sm = Hkv == 16 ? 1 : Hkv == 8 ? 2 : Hkv == 4 ? 3 : 8;
     int rc = kMaxChunk;
     const int floor = rope ? kRChunk : kMinChunk;  // the workspace holds that many splits
     while (rc > floor && (int64_t)B * n_splits(max_kv, rc) < (int64_t)kHeadsWaves * per_sm * sms)
@@ -1294,7 +1296,8 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
     Partials rpart = partials(ws, B, Hq, max_kv, rc);
     const int rsmem = Hkv * (rope ? kHStages : kHStagesPre) * 4096 + (rope ? 2 * kTabBytes : 0);
     auto kern = rope ? (Hkv == 8 ? decode_heads_kernel<8, true> : decode_heads_kernel<4, true>)
-                     : (Hkv == 8   ? decode_heads_kernel<8, false>
+                     : (Hkv == 16  ? decode_heads_kernel<16, false>
+                        : Hkv == 8 ? decode_heads_kernel<8, false>
                         : Hkv == 4 ? decode_heads_kernel<4, false>
                                    : decode_heads_kernel<2, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);

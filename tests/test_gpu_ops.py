@@ -497,11 +497,12 @@ def test_decode_rope_more_than_eight_kv_heads():
 
 
 @pytest.mark.parametrize("rope", [True, False])
-@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 8), (16, 4)])
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 8), (16, 4), (16, 2), (32, 16)])
 def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
-    """4 or 8 KV heads (one CTA per key chunk takes all KV heads; the chunk
-    partials are merged by a dependent launch), with rotation on read or
-    over a pre-rotated pool: requests with no entry, one entry, 15/16/17
+    """2, 4, 8 or 16 KV heads (one CTA per key chunk takes all KV heads -- with
+    rotation on read, for 4 and 8 -- and the chunk partials are merged by a
+    dependent launch; the other cases run the per-head kernel), with rotation
+    on read or over a pre-rotated pool: requests with no entry, one entry, 15/16/17
     entries (tile edges), many short requests, two long ones cut into many
     chunks, positions past 2^18 and a negative one, peaky scores for every
     fourth request; no fused append; two calls in a row on one workspace."""
