@@ -593,7 +593,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 }
 
 // ---------------------------------------------------------------------------
-// bf16 decode with 4 or 8 KV heads: all KV heads of a key chunk in one CTA.
+// bf16 decode, all KV heads of a key chunk in one CTA (2, 4, 8 or 16 KV
+// heads; rotation on read with 4 or 8).
 // A CTA takes (key chunk, request) with one warp per KV head (kHkv warps),
 // so the CTA reads a key's whole K and V rows.  Per head the work is the
 // per-head kernel's: 16-key tiles gathered by cp.async, the query split
@@ -624,7 +625,7 @@ constexpr int kHStagesPre = 3;
 // keys read by one 8-lane phase of a 16-byte load fall in different banks
 constexpr int kTabRow = kD / 2 + 8;
 constexpr int kTabBytes = kTileKeys * kTabRow * 8;  // one tile's cos/sin table
-constexpr int kHeadsWaves = 8;  // CTA waves (2 per SM) aimed for when choosing the chunk
+constexpr int kHeadsWaves = 8;  // CTA waves aimed for when choosing the chunk
 
 // cos/sin of pos * theta_f beyond 2^18 (the double path); rare, so out of line
 __device__ __noinline__ float2 rope_cs_wide(double theta, int pos) {
