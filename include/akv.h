@@ -355,7 +355,7 @@ akv_status akv_repos_boundary(const akv_shape *shape, const akv_oplog *ops, int3
  * host, an upper bound on any request's length (sizes the split-KV grid).
  * out [B, Hq, D] device.  A request with no keys gets zeros.
  * Limits: B <= 65535; bf16: max_kv <= 2,048,000 (AKV_ERR_UNSUPPORTED).
- * Work on `stream` (bf16): with 4 or 8 KV heads, and 2 or 16 without
+ * Work on `stream` (bf16): with 4, 8 or 16 KV heads, and 2 without
  * rotation on read, the attention launch (one CTA per key chunk and request,
  * all KV heads) and the split merge as a programmatic dependent launch;
  * otherwise a memset of B x Hkv merge counters and one launch that also

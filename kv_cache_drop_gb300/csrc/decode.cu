@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 
 // ---------------------------------------------------------------------------
 // bf16 decode, all KV heads of a key chunk in one CTA (2, 4, 8 or 16 KV
-// heads; rotation on read with 4 or 8).
+// heads; rotation on read with 4, 8 or 16).
 // A CTA takes (key chunk, request) with one warp per KV head (kHkv warps),
 // so the CTA reads a key's whole K and V rows.  Per head the work is the
 // per-head kernel's: 16-key tiles gathered by cp.async, the query split
@@ -643,9 +643,13 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 16 ? 1 : kHkv == 8 ? 2 : kH
                         const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
                         const int32_t *new_slot, int chunk, const int32_t *__restrict__ kvpos) {
   constexpr int kThreads = kHkv * 32;
-  constexpr int kTpk = kThreads / kTileKeys;  // table: threads per key
-  constexpr int kFpt = (kD / 2) / kTpk;       // table: frequencies per thread (kRope: 2 or 4)
-  constexpr int kNc4 = kFpt >= 2 ? kFpt / 2 : 1;  // float4 per thread (16 heads: no table)
+  // the angle table is filled by the first kTabThreads threads (at most 256,
+  // so that a thread computes at least two frequencies: one float4 entry)
+  constexpr int kTabThreads = kThreads < 256 ? kThreads : 256;
+  constexpr int kTpk = kTabThreads / kTileKeys;  // table: threads per key
+  constexpr int kFpt = (kD / 2) / kTpk;          // table: frequencies per thread (2, 4 or 8)
+  constexpr int kNc4 = kFpt / 2;                 // their float4 entries
+  const bool tab_thread = threadIdx.x < kTabThreads;
   constexpr int kSt = kRope ? kHStages : kHStagesPre;
   constexpr int kSB = 4096;                   // one stage: K tile 2 KiB | V tile 2 KiB
   // dynamic smem: [warp][kSt][stage], then (kRope) two cos/sin tables
@@ -734,8 +738,10 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 16 ? 1 : kHkv == 8 ? 2 : kH
   __syncthreads();  // frequencies staged, the appended row visible
   if (kRope) {
     float4 c4[kNc4];
-    angles(pos0, c4);
-    store_tab(0, c4);
+    if (tab_thread) {
+      angles(pos0, c4);
+      store_tab(0, c4);
+    }
   }
 
   uint8_t *wsm = smem + g * kSt * kSB;
@@ -885,7 +891,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 16 ? 1 : kHkv == 8 ? 2 : kH
     // the next tile's angles (stored after this tile's arithmetic)
     float4 nxt[kNc4];
     if (kRope) {
-      angles(pos1, nxt);
+      if (tab_thread) angles(pos1, nxt);
       pos1 = pos2;
       pos2 = pos3;
       pos3 = load_pos(it + 4);
@@ -946,7 +952,7 @@ __global__ void __launch_bounds__(kHkv * 32, kHkv == 16 ? 1 : kHkv == 8 ? 2 : kH
     // publish the next table; every warp is done with this one (its buffer
     // is the one the following iteration fills)
     if (kRope) {
-      if (it + 1 < n_tiles) store_tab(it + 1, nxt);
+      if (tab_thread && it + 1 < n_tiles) store_tab(it + 1, nxt);
       __syncthreads();
     } else {
       __syncwarp();
@@ -1278,11 +1284,10 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
                         const int32_t *kvpos = nullptr) {
   const int sms = device_sms();
   const bool rope = kvpos != nullptr;
-  // 4 or 8 KV heads, and 2 or 16 over a pre-rotated pool (with rotation on
+  // 4, 8 or 16 KV heads, and 2 over a pre-rotated pool (with rotation on
   // read a 2-warp CTA spreads each tile's angle table over too few threads:
-  // 5% slower than the per-head kernel there, and 22% faster without it; 16
-  // heads take 512 threads, whose table share would be one frequency each)
-  if (Hkv == 4 || Hkv == 8 || ((Hkv == 2 || Hkv == 16) && !rope)) {
+  // 5% slower than the per-head kernel there, and 22% faster without it)
+  if (Hkv == 4 || Hkv == 8 || Hkv == 16 || (Hkv == 2 && !rope)) {
     // all KV heads of a chunk in one CTA of Hkv warps (one CTA per SM for 16
     // heads, two for 8, three for 4: shared memory, eight for 2); the chunk
     // is the largest that still gives about kHeadsWaves waves of CTAs when
@@ -1296,7 +1301,9 @@ cudaError_t decode_bf16(int B, int Hq, int Hkv, const void *q, const int32_t *qp
     const int rns = n_splits(max_kv, rc);
     Partials rpart = partials(ws, B, Hq, max_kv, rc);
     const int rsmem = Hkv * (rope ? kHStages : kHStagesPre) * 4096 + (rope ? 2 * kTabBytes : 0);
-    auto kern = rope ? (Hkv == 8 ? decode_heads_kernel<8, true> : decode_heads_kernel<4, true>)
+    auto kern = rope ? (Hkv == 16  ? decode_heads_kernel<16, true>
+                        : Hkv == 8 ? decode_heads_kernel<8, true>
+                                   : decode_heads_kernel<4, true>)
                      : (Hkv == 16  ? decode_heads_kernel<16, false>
                         : Hkv == 8 ? decode_heads_kernel<8, false>
                         : Hkv == 4 ? decode_heads_kernel<4, false>

@@ -485,10 +485,11 @@ def test_decode_rope_many_splits():
     assert_close(res[0], _decode_rope_oracle(dw, 0, pos, oracle.widen(dw.q[0], "bf16")), "bf16")
 
 
-def test_decode_rope_more_than_eight_kv_heads():
-    """16 KV heads (two query heads each): more KV heads than one CTA of the
-    all-heads kernel takes, so the per-head kernel runs."""
-    dw = workloads.decode_workload(seed=33, B=3, active=(200, 4000), steps=2, Hq=32, Hkv=16)
+@pytest.mark.parametrize("Hq,Hkv", [(32, 16), (24, 3)])
+def test_decode_rope_other_kv_head_counts(Hq, Hkv):
+    """16 KV heads (the all-heads kernel with 16 warps, half of them filling
+    the angle table) and 3 (the per-head kernel)."""
+    dw = workloads.decode_workload(seed=33, B=3, active=(200, 4000), steps=2, Hq=Hq, Hkv=Hkv)
     pos = _rope_positions(dw, seed=34)
     res, _, _ = _run_decode_rope(dw, {0, 1}, pos)
     for step, got in res.items():
@@ -500,9 +501,9 @@ def test_decode_rope_more_than_eight_kv_heads():
 @pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 8), (16, 4), (16, 2), (32, 16)])
 def test_decode_edges_all_heads_kernel(Hq, Hkv, rope):
     """2, 4, 8 or 16 KV heads (one CTA per key chunk takes all KV heads -- with
-    rotation on read, for 4 and 8 -- and the chunk partials are merged by a
-    dependent launch; the other cases run the per-head kernel), with rotation
-    on read or over a pre-rotated pool: requests with no entry, one entry, 15/16/17
+    rotation on read, for 4, 8 and 16 -- and the chunk partials are merged by
+    a dependent launch; the other case runs the per-head kernel), with
+    rotation on read or over a pre-rotated pool: requests with no entry, one entry, 15/16/17
     entries (tile edges), many short requests, two long ones cut into many
     chunks, positions past 2^18 and a negative one, peaky scores for every
     fourth request; no fused append; two calls in a row on one workspace."""
